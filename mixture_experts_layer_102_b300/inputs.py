@@ -1,0 +1,107 @@
+"""Seeded synthetic inputs for the MoE FFN layer, shared by the CUDA path's tests,
+the benchmark and the oracle's tests.
+
+The recipe (one numpy PCG64 stream per tensor, spawned from ``SeedSequence(seed)`` in
+the order x, router weight, router bias, W1, W3, W2):
+
+* x[T,H] ~ N(0, 1)
+* router weight W_r[H,N] ~ N(0, 0.02**2)          (std 0.02)
+* W1[N,F,H], W3[N,F,H] ~ N(0, 1/H)                 (std = fan_in**-0.5, fan_in = H)
+* W2[N,H,F] ~ N(0, 1/F)                            (std = fan_in**-0.5, fan_in = F)
+* optional router bias b[N] = 2.0 * r**-1.1 with r a seeded permutation of 1..N, so
+  the hottest expert gets exactly +2.0 (a Zipf(1.1) profile scaled to 2.0 max).
+
+Values are drawn as float32 normals. For bf16 workloads every tensor except the
+bias is rounded to bf16 (round to nearest even) and the rounded values are what both
+the GPU path and the oracle consume. Expert weights use the ``nn.Linear`` [out, in]
+orientation, so W1/W3 rows are indexed by the SwiGLU column f and W2 rows by the
+hidden column h.
+
+This module draws numbers and converts storage formats; it holds none of the layer's
+arithmetic.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+from typing import Optional
+
+import numpy as np
+
+from .configs import MoEConfig
+
+
+def f32_to_bf16_bits(a: np.ndarray) -> np.ndarray:
+    """Round finite float32 values to bf16 (nearest, ties to even); return the bits."""
+    u = np.ascontiguousarray(a, dtype=np.float32).view(np.uint32)
+    lsb = (u >> np.uint32(16)) & np.uint32(1)
+    return ((u + np.uint32(0x7FFF) + lsb) >> np.uint32(16)).astype(np.uint16)
+
+
+def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
+    """Widen bf16 bit patterns to the float32 values they encode (exact)."""
+    return (np.ascontiguousarray(bits, dtype=np.uint16).astype(np.uint32)
+            << np.uint32(16)).view(np.float32)
+
+
+@dataclass
+class MoEInputs:
+    """Storage arrays of one layer instance.
+
+    For ``dtype == "bf16"`` the arrays x, w_router, w1, w3, w2 hold uint16 bf16 bit
+    patterns; for ``"f32"`` they hold float32. ``router_bias`` is float32 or None.
+    """
+    dtype: str
+    x: np.ndarray
+    w_router: np.ndarray
+    router_bias: Optional[np.ndarray]
+    w1: np.ndarray
+    w3: np.ndarray
+    w2: np.ndarray
+
+    def values(self, name: str) -> np.ndarray:
+        """float32 values of a storage array (bf16 bits widened exactly)."""
+        a = getattr(self, name)
+        if a is None:
+            return None
+        if self.dtype == "bf16" and a.dtype == np.uint16:
+            return bf16_bits_to_f32(a)
+        return a
+
+
+def _normal(seq: np.random.SeedSequence, shape, std: float) -> np.ndarray:
+    g = np.random.Generator(np.random.PCG64(seq))
+    out = g.standard_normal(size=shape, dtype=np.float32)
+    if std != 1.0:
+        out *= np.float32(std)
+    return out
+
+
+def _store(a: np.ndarray, dtype: str) -> np.ndarray:
+    return f32_to_bf16_bits(a) if dtype == "bf16" else a
+
+
+def make_x(cfg: MoEConfig, rank: int = 0) -> np.ndarray:
+    """Activations only. Rank 0 uses the workload's own x stream; rank r > 0 of a
+    data-parallel run draws an independent batch from ``SeedSequence([seed, 1000+r])``."""
+    seqs = np.random.SeedSequence(cfg.seed).spawn(6)
+    seq = seqs[0] if rank == 0 else np.random.SeedSequence([cfg.seed, 1000 + rank])
+    return _store(_normal(seq, (cfg.T, cfg.H), 1.0), cfg.dtype)
+
+
+def make_inputs(cfg: MoEConfig, rank: int = 0, with_experts: bool = True) -> MoEInputs:
+    seqs = np.random.SeedSequence(cfg.seed).spawn(6)
+    T, H, N, F = cfg.T, cfg.H, cfg.N, cfg.F
+    x = make_x(cfg, rank)
+    w_router = _store(_normal(seqs[1], (H, N), 0.02), cfg.dtype)
+    bias = None
+    if cfg.zipf_bias:
+        g = np.random.Generator(np.random.PCG64(seqs[2]))
+        r = g.permutation(N).astype(np.float64) + 1.0
+        bias = (2.0 * r ** -1.1).astype(np.float32)
+    if with_experts:
+        w1 = _store(_normal(seqs[3], (N, F, H), H ** -0.5), cfg.dtype)
+        w3 = _store(_normal(seqs[4], (N, F, H), H ** -0.5), cfg.dtype)
+        w2 = _store(_normal(seqs[5], (N, H, F), F ** -0.5), cfg.dtype)
+    else:
+        w1 = w3 = w2 = None
+    return MoEInputs(cfg.dtype, x, w_router, bias, w1, w3, w2)

@@ -1,0 +1,239 @@
+"""Plain CPU fp64 oracle of the forward pass of one top-k routed MoE FFN layer.
+
+TEST INFRASTRUCTURE ONLY. Only the tests, the smoke check and the benchmark's CPU
+baseline leg import this module. The product path (the CUDA library and its Python
+binding) never calls it, and it shares no code with that path: it receives plain
+arrays (the same bf16-rounded values the GPU gets, as float32) and widens them to
+float64 itself.
+
+What it computes, step by step, in the pages' order:
+
+1. router logits  l = x @ W_r (+ b)           -- a small linear layer [hidden, N]
+   (cf-1.com/news/5914943 section 2.1; 2kiu.com/news/2885792 section 3.1)
+2. full router softmax P = softmax(l)          -- used only by the aux loss
+   (cf-1.com/news/5914943 section 2.3; devpress.csdn.net MoE page section 4.1)
+3. top-k over the logits, ties to the lower expert id, then a softmax over the k
+   selected logits (cf-1.com/news/5914943 section 2.1; hotelren.com/news/3071227
+   section 4.1; stable tie order: 2kiu.com/news/2885792 section 5.3)
+4. aux = N * sum_e f_e * P_e with f_e the fraction of routing slots sent to e and P_e
+   the mean router probability of e (cf-1.com/news/5914943 section 2.3)
+5. per-expert capacity C = ceil(CF*T*k/N); each expert keeps the first C routed tokens
+   in token order and drops the rest to the residual (cf-1.com/news/5914943 section
+   2.3 note; 2kiu.com/news/2885792 sections 2.2 and 3.1)
+6. each kept slot runs the expert's SwiGLU FFN  W2 (silu(W1 x) * (W3 x))
+   (2kiu.com/news/2885792 section 2.2 names SwiGLU as the expert FFN)
+7. combine y[t] = sum over kept slots of w[t,s] * expert output
+   (cf-1.com/news/5914943 section 2.1; hotelren.com/news/5904824 section 3.1)
+
+Readings where the pages are open (each also listed in the design notes):
+* f_e = counts_e / (T*k), so sum_e f_e = 1 and a balanced router gives aux = 1 (the
+  pages say the ideal value is about 1); counts are taken BEFORE capacity.
+* C = ceil(CF*T*k/N) evaluated in IEEE double from the float32 value of CF.
+  capacity_factor None (or <= 0) means no limit.
+* a dropped slot contributes 0 and the kept slots keep their original gate weights
+  (no renormalisation); the layer returns only the MoE branch, the caller adds the
+  residual, so a token with every slot dropped gets exactly 0.
+* T = 0 gives aux = 0 (empty sums).
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass
+from typing import Optional
+
+import numpy as np
+
+NEAR_TIE_MARGIN = 1e-4
+
+
+def capacity(T: int, k: int, N: int, capacity_factor: Optional[float]) -> Optional[int]:
+    """Per-expert capacity C = ceil(CF*T*k/N), or None for no limit.
+
+    CF is the layer's float32 value; the product is evaluated left to right in
+    double: ((CF*T)*k)/N.
+    """
+    if capacity_factor is None or capacity_factor <= 0:
+        return None
+    cf = float(np.float32(capacity_factor))
+    return int(math.ceil(cf * T * k / N))
+
+
+def capacity_page_example_variant(num_tokens: int, num_experts: int, cf: float) -> int:
+    """The worked capacity example's own formula: floor(CF * tokens / experts), with
+    no top-k factor (hotelren.com/news/3071227 section 2.2). Not used by the layer;
+    it only reproduces the page's printed numbers."""
+    return int(math.floor(cf * num_tokens / num_experts))
+
+
+def router_logits(x: np.ndarray, w_router: np.ndarray,
+                  bias: Optional[np.ndarray] = None) -> np.ndarray:
+    """l[t,e] = sum_h x[t,h] * W_r[h,e] (+ b[e]), in float64."""
+    l = np.asarray(x, np.float64) @ np.asarray(w_router, np.float64)
+    if bias is not None:
+        l = l + np.asarray(bias, np.float64)[None, :]
+    return l
+
+
+def full_softmax(logits: np.ndarray) -> np.ndarray:
+    """Row-wise softmax over all N experts (max subtracted first)."""
+    m = logits.max(axis=1, keepdims=True) if logits.shape[0] else 0.0
+    e = np.exp(logits - m)
+    return e / e.sum(axis=1, keepdims=True)
+
+
+def topk_select(logits: np.ndarray, k: int) -> np.ndarray:
+    """Indices of the k largest logits per token, ordered by logit descending; equal
+    logits are ordered by ascending expert id (the stable tie rule)."""
+    T, N = logits.shape
+    ids = np.broadcast_to(np.arange(N), (T, N))
+    # np.lexsort sorts by the LAST key first: primary -logit, secondary id.
+    order = np.lexsort((ids, -logits), axis=-1)
+    return order[:, :k].astype(np.int64)
+
+
+def gate_weights(logits: np.ndarray, idx: np.ndarray) -> np.ndarray:
+    """Softmax over the k selected logits of each token."""
+    sel = np.take_along_axis(logits, idx, axis=1)
+    e = np.exp(sel - sel[:, :1]) if sel.shape[0] else sel
+    return e / e.sum(axis=1, keepdims=True)
+
+
+def expert_counts(idx: np.ndarray, N: int) -> np.ndarray:
+    """Number of routing slots sent to each expert (before capacity)."""
+    return np.bincount(idx.ravel(), minlength=N).astype(np.int64)
+
+
+def aux_loss(probs: np.ndarray, idx: np.ndarray, N: int, k: int) -> float:
+    """aux = N * sum_e f_e * P_e, f_e = counts_e/(T*k), P_e = mean_t P[t,e]."""
+    T = idx.shape[0]
+    if T == 0:
+        return 0.0
+    f = expert_counts(idx, N) / float(T * k)
+    P = probs.mean(axis=0)
+    return float(N * np.sum(f * P))
+
+
+def capacity_assign(idx: np.ndarray, N: int, C: Optional[int]):
+    """Walk the slots in token order (t ascending, then slot s) and give each the
+    number of earlier slots that chose the same expert. A slot is dropped when that
+    rank reaches C. Returns (rank[T,k], drop_mask[T,k] uint8, kept_counts[N])."""
+    T, k = idx.shape
+    rank = np.zeros((T, k), dtype=np.int64)
+    seen = [0] * N
+    for t in range(T):
+        for s in range(k):
+            e = int(idx[t, s])
+            rank[t, s] = seen[e]
+            seen[e] += 1
+    if C is None:
+        drop = np.zeros((T, k), dtype=np.uint8)
+    else:
+        drop = (rank >= C).astype(np.uint8)
+    kept = np.zeros(N, dtype=np.int64)
+    np.add.at(kept, idx[drop == 0], 1)
+    return rank, drop, kept
+
+
+def silu(z: np.ndarray) -> np.ndarray:
+    """silu(z) = z * sigmoid(z) = z / (1 + exp(-z))."""
+    with np.errstate(over="ignore"):
+        return z / (1.0 + np.exp(-z))
+
+
+def swiglu_expert(x_rows: np.ndarray, w1_e: np.ndarray, w3_e: np.ndarray,
+                  w2_e: np.ndarray) -> np.ndarray:
+    """One expert: W2 (silu(W1 x) * (W3 x)), weights in [out, in] orientation."""
+    xr = np.asarray(x_rows, np.float64)
+    g = xr @ np.asarray(w1_e, np.float64).T
+    u = xr @ np.asarray(w3_e, np.float64).T
+    return (silu(g) * u) @ np.asarray(w2_e, np.float64).T
+
+
+def near_tie_tokens(logits: np.ndarray, k: int, margin: float = NEAR_TIE_MARGIN):
+    """(set_ties, order_ties): tokens whose k-th and (k+1)-th largest logits differ by
+    less than ``margin`` (the selected SET may flip), and tokens where two
+    consecutive selected logits do (only the slot ORDER may flip)."""
+    T, N = logits.shape
+    s = -np.sort(-logits, axis=1)
+    if k < N:
+        set_ties = np.nonzero(s[:, k - 1] - s[:, k] < margin)[0]
+    else:
+        set_ties = np.zeros(0, dtype=np.int64)
+    if k > 1:
+        order_ties = np.nonzero((s[:, :k - 1] - s[:, 1:k] < margin).any(axis=1))[0]
+    else:
+        order_ties = np.zeros(0, dtype=np.int64)
+    return set_ties, order_ties
+
+
+def active_fraction(idx: np.ndarray, N: int) -> float:
+    """Mean fraction of the N experts whose FFN a token runs (distinct experts)."""
+    if idx.shape[0] == 0:
+        return 0.0
+    return float(np.mean([len(set(row.tolist())) for row in idx]) / N)
+
+
+@dataclass
+class OracleResult:
+    logits: np.ndarray          # [T,N] float64
+    probs: np.ndarray           # [T,N] float64
+    topk_idx: np.ndarray        # [T,k] int64
+    topk_w: np.ndarray          # [T,k] float64
+    aux_loss: float
+    expert_counts: np.ndarray   # [N] before capacity
+    capacity: Optional[int]
+    rank: np.ndarray            # [T,k]
+    drop_mask: np.ndarray       # [T,k] uint8, 1 = dropped
+    kept_counts: np.ndarray     # [N]
+    tokens: np.ndarray          # token ids whose output rows are in ``out``
+    out: np.ndarray             # [len(tokens), H] float64
+    near_tie_set: np.ndarray
+    near_tie_order: np.ndarray
+
+
+def route(x, w_router, bias, k: int, capacity_factor):
+    """Steps 1-5 for every token."""
+    T = x.shape[0]
+    N = w_router.shape[1]
+    logits = router_logits(x, w_router, bias)
+    probs = full_softmax(logits)
+    idx = topk_select(logits, k)
+    w = gate_weights(logits, idx)
+    aux = aux_loss(probs, idx, N, k)
+    counts = expert_counts(idx, N)
+    C = capacity(T, k, N, capacity_factor)
+    rank, drop, kept = capacity_assign(idx, N, C)
+    set_ties, order_ties = near_tie_tokens(logits, k)
+    return dict(logits=logits, probs=probs, topk_idx=idx, topk_w=w, aux_loss=aux,
+                expert_counts=counts, capacity=C, rank=rank, drop_mask=drop,
+                kept_counts=kept, near_tie_set=set_ties, near_tie_order=order_ties)
+
+
+def moe_forward(x, w_router, bias, w1, w3, w2, k: int, capacity_factor,
+                token_sample: Optional[np.ndarray] = None) -> OracleResult:
+    """The whole layer. Routing and capacity always cover every token (capacity
+    depends on token order); the expert FFN and the combine are evaluated for the
+    tokens in ``token_sample`` (all tokens when None)."""
+    T, H = x.shape
+    N = w_router.shape[1]
+    r = route(x, w_router, bias, k, capacity_factor)
+    tokens = np.arange(T) if token_sample is None else np.asarray(token_sample, np.int64)
+    out = np.zeros((len(tokens), H), dtype=np.float64)
+    idx, w, drop = r["topk_idx"], r["topk_w"], r["drop_mask"]
+    # Queue every kept slot of the requested tokens on its expert.
+    queue = [([], []) for _ in range(N)]
+    for i, t in enumerate(tokens):
+        for s in range(k):
+            if not drop[t, s]:
+                queue[int(idx[t, s])][0].append(i)
+                queue[int(idx[t, s])][1].append(s)
+    for e in range(N):
+        rows, slots = queue[e]
+        if not rows:
+            continue
+        rows = np.asarray(rows)
+        slots = np.asarray(slots)
+        # A token visits an expert at most once, so ``rows`` has no repeats here.
+        ye = swiglu_expert(np.asarray(x[tokens[rows]], np.float64), w1[e], w3[e], w2[e])
+        out[rows] += w[tokens[rows], slots][:, None] * ye
+    return OracleResult(out=out, tokens=tokens, **r)

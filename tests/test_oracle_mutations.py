@@ -1,0 +1,123 @@
+"""Plant plausible mistakes in the oracle (CPU only) and check that the pins catch
+each one. A pin that still passes with the mistake planted would not be pinning."""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+import oracle.moe_oracle as om
+import test_oracle_pins as pins
+
+
+def _plant(monkeypatch, name, fn):
+    monkeypatch.setattr(om, name, fn)
+    monkeypatch.setattr(oracle, name, fn)
+
+
+def _fails(test, *args):
+    with pytest.raises(AssertionError):
+        test(*args)
+
+
+def test_capacity_floor_instead_of_ceil_is_caught(monkeypatch):
+    def floor_cap(T, k, N, cf):
+        if cf is None or cf <= 0:
+            return None
+        return int(math.floor(float(np.float32(cf)) * T * k / N))
+    _plant(monkeypatch, "capacity", floor_cap)
+    _fails(pins.test_capacity_named_workloads_closed_form)
+
+
+def test_capacity_without_topk_factor_is_caught(monkeypatch):
+    def no_k(T, k, N, cf):
+        if cf is None or cf <= 0:
+            return None
+        return int(math.ceil(float(np.float32(cf)) * T / N))
+    _plant(monkeypatch, "capacity", no_k)
+    _fails(pins.test_capacity_named_workloads_closed_form)
+
+
+def test_aux_without_division_by_k_is_caught(monkeypatch):
+    def aux_no_k(probs, idx, N, k):
+        T = idx.shape[0]
+        f = om.expert_counts(idx, N) / float(T)
+        return float(N * np.sum(f * probs.mean(axis=0)))
+    _plant(monkeypatch, "aux_loss", aux_no_k)
+    _fails(pins.test_aux_is_one_for_a_zero_router, 8, 2)
+
+
+def test_aux_after_capacity_is_caught(monkeypatch):
+    real_route = om.route
+
+    def route_post_cap(x, w_router, bias, k, cf):
+        r = real_route(x, w_router, bias, k, cf)
+        T, N = r["logits"].shape
+        if T:
+            f = r["kept_counts"] / float(T * k)
+            r["aux_loss"] = float(N * np.sum(f * r["probs"].mean(axis=0)))
+        return r
+    _plant(monkeypatch, "route", route_post_cap)
+    _fails(pins.test_aux_uses_counts_before_capacity)
+
+
+def test_reversed_tie_rule_is_caught(monkeypatch):
+    def topk_high_id(logits, k):
+        T, N = logits.shape
+        ids = np.broadcast_to(np.arange(N), (T, N))
+        return np.lexsort((-ids, -logits), axis=-1)[:, :k]
+    _plant(monkeypatch, "topk_select", topk_high_id)
+    _fails(pins.test_topk_brute_force_with_ties)
+
+
+def test_gate_softmax_over_all_experts_is_caught(monkeypatch):
+    def gate_all(logits, idx):
+        p = om.full_softmax(logits)
+        return np.take_along_axis(p, idx, axis=1)
+    _plant(monkeypatch, "gate_weights", gate_all)
+    _fails(pins.test_gate_weights_sum_to_one_and_equal_renormalised_probs)
+
+
+def test_swapped_w1_w3_is_caught(monkeypatch):
+    real = om.swiglu_expert
+    _plant(monkeypatch, "swiglu_expert", lambda x, w1, w3, w2: real(x, w3, w1, w2))
+    _fails(pins.test_swiglu_orientation_with_one_hot_weights)
+
+
+def test_silu_sign_error_is_caught(monkeypatch):
+    _plant(monkeypatch, "silu", lambda z: z / (1.0 + np.exp(z)))
+    _fails(pins.test_silu_against_library_sigmoid)
+
+
+def test_capacity_priority_reversed_is_caught(monkeypatch):
+    real = om.capacity_assign
+
+    def latest_first(idx, N, C):
+        rank, drop, kept = real(idx[::-1].copy(), N, C)
+        return rank[::-1].copy(), drop[::-1].copy(), kept
+    _plant(monkeypatch, "capacity_assign", latest_first)
+    _fails(pins.test_capacity_invariants, 0.5)
+
+
+def test_renormalising_after_a_drop_is_caught(monkeypatch):
+    real_route = om.route
+
+    def route_renorm(x, w_router, bias, k, cf):
+        r = real_route(x, w_router, bias, k, cf)
+        w = r["topk_w"] * (1 - r["drop_mask"])
+        s = w.sum(axis=1, keepdims=True)
+        r["topk_w"] = np.where(s > 0, w / np.where(s > 0, s, 1.0), 0.0)
+        return r
+    _plant(monkeypatch, "route", route_renorm)
+    _fails(pins.test_dropped_slots_give_zero_and_kept_weights_are_not_renormalised)
+
+
+def test_ignoring_drops_in_the_combine_is_caught(monkeypatch):
+    real_route = om.route
+
+    def route_no_drop(x, w_router, bias, k, cf):
+        r = real_route(x, w_router, bias, k, cf)
+        r["drop_mask"] = np.zeros_like(r["drop_mask"])
+        return r
+    _plant(monkeypatch, "route", route_no_drop)
+    _fails(pins.test_dropped_slots_give_zero_and_kept_weights_are_not_renormalised)
