@@ -1,0 +1,165 @@
+/*
+ * moe.h -- C ABI of the B300 (sm_103a) forward pass of one top-k routed
+ * Mixture-of-Experts FFN layer.
+ *
+ * The layer, as the pages state it:
+ *   logits = x @ W_r (+ b)                  router: a small linear layer [hidden, N]
+ *   idx, w = top-k(logits), softmax over the k selected logits
+ *   aux    = N * sum_e f_e * P_e            load-balancing loss
+ *   C      = ceil(CF * T * k / N)           per-expert capacity; overflow is dropped
+ *   y[t]   = sum over kept slots s of w[t,s] * W2_e (silu(W1_e x_t) * (W3_e x_t))
+ * Sources: cf-1.com/news/5914943 sections 2.1 (router, top-k, softmax, weighted
+ * sum) and 2.3 (aux loss, capacity note); 2kiu.com/news/2885792 sections 2.2
+ * (SwiGLU experts, capacity factor) and 3.1 (hard top-k with capacity, first
+ * tokens kept); hotelren.com/news/3071227 section 4.1 (router returns indices,
+ * weights, mask); 2kiu.com/news/2885792 section 5.3 (equal logits ordered by
+ * ascending expert id).
+ *
+ * Conventions shared by every entry point:
+ *  - All tensor pointers are DEVICE pointers on the current CUDA device, row-major
+ *    and densely packed, 16-byte aligned. The caller owns and allocates every
+ *    buffer, including the workspace; the library allocates no device memory and
+ *    keeps no state between calls.
+ *  - Element type of x, w_router, w1, w3, w2, out: float32 (MOE_F32) or bf16
+ *    (MOE_BF16) as cfg->dtype says. router_bias is always float32.
+ *  - Shapes: x [T,H]; w_router [H,N]; router_bias [N]; w1, w3 [N,F,H] and
+ *    w2 [N,H,F] (nn.Linear [out,in] orientation per expert); out [T,H];
+ *    topk_idx [T,k] int32; topk_w [T,k] float32; drop_mask [T,k] uint8
+ *    (1 = slot dropped by capacity); expert_counts, kept_counts [N] int32;
+ *    aux_loss [1] float32.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
+ *    stream). A return of MOE_OK means the work was enqueued. Arguments are
+ *    checked on the host before anything is enqueued; a failed check enqueues
+ *    nothing and touches no CUDA API.
+ *  - Kernels report device-side failures (a bounded wait that gave up, an index
+ *    out of range) by OR-ing bits into a status word inside the workspace;
+ *    moe_get_status() reads and clears it.
+ *  - Calls sharing one workspace must not overlap on the GPU (use one stream).
+ *  - Supported: 1 <= k <= min(N, 32), 1 <= N <= 256, T >= 0, H and F multiples
+ *    of 64. The library is built for sm_103a only.
+ */
+#ifndef MOE_B300_H
+#define MOE_B300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum {
+  MOE_OK = 0,
+  MOE_EINVAL = 1,        /* NULL required pointer, negative size, k > N, bad dtype */
+  MOE_EUNSUPPORTED = 2,  /* a valid layer outside the supported range above */
+  MOE_EWORKSPACE = 3,    /* workspace NULL, misaligned or smaller than moe_workspace_size */
+  MOE_EALIGN = 4,        /* a tensor pointer that is not 16-byte aligned */
+  MOE_ECUDA = 5,         /* a CUDA runtime call or a kernel launch failed */
+  MOE_EDEVICE = 6,       /* a kernel set the workspace status word */
+  MOE_ENODEVICE = 7      /* the current device is not an sm_103 GPU */
+};
+
+typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype;
+
+/* One layer instance. capacity_factor <= 0 means no capacity limit. */
+typedef struct {
+  int32_t T;                 /* tokens (batch * seq_len) */
+  int32_t H;                 /* hidden size */
+  int32_t N;                 /* routed experts */
+  int32_t k;                 /* experts per token */
+  int32_t F;                 /* SwiGLU inner width of one expert */
+  float capacity_factor;     /* CF of C = ceil(CF*T*k/N) */
+  int32_t dtype;             /* moe_dtype */
+} moe_cfg;
+
+/* Number of stages moe_forward_timed() brackets with events. */
+#define MOE_NUM_STAGES 8
+
+/*
+ * Bytes of device workspace moe_route / moe_forward need for `cfg`; 0 if cfg is
+ * invalid or unsupported. Pure host function; the size grows linearly in T*k*(H+F).
+ */
+size_t moe_workspace_size(const moe_cfg* cfg);
+
+/*
+ * Per-expert capacity C = ceil(CF*T*k/N) (2kiu.com/news/2885792 section 3.1 keeps
+ * the first C tokens of each expert; cf-1.com/news/5914943 section 2.3 sends the
+ * overflow to the residual). CF is the float32 value of cfg->capacity_factor and
+ * the product is evaluated in double as ((CF*T)*k)/N. Writes -1 when there is no
+ * limit. Pure host function. Returns MOE_OK or MOE_EINVAL.
+ */
+int moe_capacity(const moe_cfg* cfg, int64_t* capacity);
+
+/*
+ * Zero the workspace's status word (call once after allocating a workspace whose
+ * contents are unknown). Asynchronous on `stream`.
+ */
+int moe_workspace_init(void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Routing half of the layer (hotelren.com/news/3071227 section 4.1: the router
+ * returns expert indices, weights and a mask):
+ *   topk_idx[t,s]  the s-th largest logit's expert (ties: lower expert id first)
+ *   topk_w[t,s]    softmax over the k selected logits
+ *   aux_loss[0]    N * sum_e (counts_e/(T*k)) * (sum_t P[t,e] / T), P the softmax
+ *                  over all N logits, counts taken before capacity (T = 0 gives 0)
+ *   drop_mask[t,s] 1 when the slot's rank among the expert's slots, in token order,
+ *                  is >= C
+ *   expert_counts  slots per expert before capacity (optional, NULL ok)
+ *   kept_counts    slots per expert after capacity (optional, NULL ok)
+ * router_bias may be NULL (no bias). Required: x, w_router, topk_idx, topk_w,
+ * aux_loss, drop_mask, workspace.
+ */
+int moe_route(const moe_cfg* cfg, const void* x, const void* w_router,
+              const float* router_bias, int32_t* topk_idx, float* topk_w,
+              float* aux_loss, uint8_t* drop_mask, int32_t* expert_counts,
+              int32_t* kept_counts, void* workspace, size_t workspace_bytes,
+              void* stream);
+
+/*
+ * The whole layer forward: routing as in moe_route, then each kept slot runs its
+ * expert's SwiGLU FFN W2 (silu(W1 x) * (W3 x)) (2kiu.com/news/2885792 section 2.2)
+ * and out[t] = sum over kept slots of topk_w[t,s] * expert output
+ * (cf-1.com/news/5914943 section 2.1). Dropped slots contribute 0 and the kept
+ * slots keep their weights; the residual is NOT added (the caller adds x), so a
+ * token whose every slot was dropped gets out = 0. Required: x, w_router, w1, w3,
+ * w2, out, workspace. Optional (NULL ok): router_bias and the routing outputs.
+ */
+int moe_forward(const moe_cfg* cfg, const void* x, const void* w_router,
+                const float* router_bias, const void* w1, const void* w3,
+                const void* w2, void* out, int32_t* topk_idx, float* topk_w,
+                float* aux_loss, uint8_t* drop_mask, int32_t* expert_counts,
+                int32_t* kept_counts, void* workspace, size_t workspace_bytes,
+                void* stream);
+
+/*
+ * moe_forward with stage timing: `stage_events` holds MOE_NUM_STAGES+1 cudaEvent_t
+ * handles created by the caller; event i is recorded on `stream` before stage i and
+ * event MOE_NUM_STAGES after the last stage. Stages: 0 router logits, 1 router
+ * top-k/softmax, 2 capacity count, 3 capacity scan and aux, 4 dispatch (permute),
+ * 5 expert GEMM1 + SwiGLU, 6 expert GEMM2, 7 gated combine. NULL stage_events
+ * behaves as moe_forward.
+ */
+int moe_forward_timed(const moe_cfg* cfg, const void* x, const void* w_router,
+                      const float* router_bias, const void* w1, const void* w3,
+                      const void* w2, void* out, int32_t* topk_idx, float* topk_w,
+                      float* aux_loss, uint8_t* drop_mask, int32_t* expert_counts,
+                      int32_t* kept_counts, void* workspace, size_t workspace_bytes,
+                      void* stream, void* const* stage_events);
+
+/*
+ * Synchronise `stream`, read and clear the workspace status word. Returns MOE_OK,
+ * MOE_EDEVICE (a kernel reported a failure; *bits, if not NULL, gets the word) or
+ * MOE_ECUDA. Bits: 1 a bounded wait gave up, 2 an index out of range.
+ */
+int moe_get_status(void* workspace, size_t workspace_bytes, void* stream,
+                   uint32_t* bits);
+
+/* Static description of a status code. */
+const char* moe_strerror(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_B300_H */

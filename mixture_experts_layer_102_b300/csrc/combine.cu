@@ -1,0 +1,63 @@
+// Gate-weighted combine: out[t] = sum over kept slots s of w[t,s] * ye[row(t,s)]
+// (cf-1.com/news/5914943 section 2.1: "weighted sum of the k experts' outputs";
+// devpress.csdn.net MoE page section 4.1: gather the expert results back into token
+// order). Dropped slots contribute nothing and the kept slots keep their weights;
+// the residual is added by the caller (cf-1.com/news/5914943 section 2.3 note).
+//
+// One warp per token, 16-byte vectors, fp32 accumulation in a fixed slot order so
+// the result does not depend on scheduling.
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+namespace {
+
+template <typename TIo>
+__global__ void __launch_bounds__(256)
+combine_kernel(const TIo* __restrict__ ye, const int32_t* __restrict__ slot_row,
+               const float* __restrict__ w, int T, int k, int H, TIo* __restrict__ out) {
+  __shared__ int32_t rows[8][32];
+  __shared__ float wts[8][32];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * 8 + warp;
+  if (t >= T) return;
+  if (lane < k) {
+    rows[warp][lane] = slot_row[(size_t)t * k + lane];
+    wts[warp][lane] = w[(size_t)t * k + lane];
+  }
+  __syncwarp();
+  const int nvec = H / 8;
+  for (int v = lane; v < nvec; v += 32) {
+    float acc[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) acc[q] = 0.f;
+    for (int s = 0; s < k; ++s) {
+      const int r = rows[warp][s];
+      if (r < 0) continue;
+      const float ws = wts[warp][s];
+      float val[8];
+      load8(ye + (size_t)r * H + v * 8, val);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) acc[q] = fmaf(ws, val[q], acc[q]);
+    }
+    store8(out + (size_t)t * H + v * 8, acc);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_combine(int dtype, const void* ye, const int32_t* slot_row, const float* w,
+                           int T, int k, int H, void* out, cudaStream_t stream) {
+  if (T == 0) return cudaSuccess;
+  const int blocks = (T + 7) / 8;
+  if (dtype == 1)
+    combine_kernel<__nv_bfloat16><<<blocks, 256, 0, stream>>>(
+        static_cast<const __nv_bfloat16*>(ye), slot_row, w, T, k, H,
+        static_cast<__nv_bfloat16*>(out));
+  else
+    combine_kernel<float><<<blocks, 256, 0, stream>>>(static_cast<const float*>(ye), slot_row, w,
+                                                      T, k, H, static_cast<float*>(out));
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,104 @@
+// float32 grouped expert GEMM on CUDA cores, used when the layer's dtype is float32:
+// fp32 FMA throughout (no TF32), so the result stays within fp32 rounding of the
+// exact product. Expert e's rows are [offsets[e], offsets[e+1]) of the permuted
+// buffer, visited as 128-row tiles from the tile table the capacity scan writes.
+//
+//   swiglu: out = silu(A W1_e^T) * (A W3_e^T)   (2kiu.com/news/2885792 section 2.2)
+//   plain:  out = A W2_e^T
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+namespace {
+
+constexpr int BM = GEMM_BM;  // 128 rows
+constexpr int BN = 64;       // output columns per block
+constexpr int BK = 16;
+
+template <bool SWIGLU>
+__global__ void __launch_bounds__(256)
+gemm_simt_kernel(const float* __restrict__ A, const float* __restrict__ B0,
+                 const float* __restrict__ B1, float* __restrict__ out, int K, int n_cols,
+                 const int32_t* __restrict__ tile_expert, const int32_t* __restrict__ tile_row0,
+                 const int32_t* __restrict__ offsets, const int32_t* __restrict__ num_mtiles) {
+  const int mt = blockIdx.x;
+  if (mt >= *num_mtiles) return;
+  const int e = tile_expert[mt];
+  const int r0 = tile_row0[mt];
+  const int rend = offsets[e + 1];
+  const int n0 = blockIdx.y * BN;
+  __shared__ float As[BK][BM + 4];
+  __shared__ float Bs0[BK][BN + 4];
+  __shared__ float Bs1[SWIGLU ? BK : 1][BN + 4];
+  const float* Be0 = B0 + (size_t)e * n_cols * K;
+  const float* Be1 = SWIGLU ? B1 + (size_t)e * n_cols * K : nullptr;
+  const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;  // rows ty*8.., cols tx*4..
+  float acc0[8][4], acc1[8][4];
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc0[i][j] = acc1[i][j] = 0.f;
+
+  for (int k0 = 0; k0 < K; k0 += BK) {
+    for (int l = tid; l < BM * BK; l += 256) {
+      const int r = l / BK, kk = l - r * BK;
+      As[kk][r] = (r0 + r < rend) ? A[(size_t)(r0 + r) * K + k0 + kk] : 0.f;
+    }
+    for (int l = tid; l < BN * BK; l += 256) {
+      const int n = l / BK, kk = l - n * BK;
+      const bool ok = n0 + n < n_cols;
+      Bs0[kk][n] = ok ? Be0[(size_t)(n0 + n) * K + k0 + kk] : 0.f;
+      if (SWIGLU) Bs1[kk][n] = ok ? Be1[(size_t)(n0 + n) * K + k0 + kk] : 0.f;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int kk = 0; kk < BK; ++kk) {
+      float av[8], b0[4], b1[4];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) av[i] = As[kk][ty * 8 + i];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        b0[j] = Bs0[kk][tx * 4 + j];
+        b1[j] = SWIGLU ? Bs1[kk][tx * 4 + j] : 0.f;
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          acc0[i][j] = fmaf(av[i], b0[j], acc0[i][j]);
+          if (SWIGLU) acc1[i][j] = fmaf(av[i], b1[j], acc1[i][j]);
+        }
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int r = r0 + ty * 8 + i;
+    if (r >= rend) continue;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int c = n0 + tx * 4 + j;
+      if (c < n_cols) out[(size_t)r * n_cols + c] = SWIGLU ? silu(acc0[i][j]) * acc1[i][j] : acc0[i][j];
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_grouped_gemm_simt(const GroupedGemmArgs& a, cudaStream_t stream) {
+  if (a.max_mtiles == 0) return cudaSuccess;
+  const dim3 grid(a.max_mtiles, (a.n_cols + BN - 1) / BN);
+  if (a.swiglu)
+    gemm_simt_kernel<true><<<grid, 256, 0, stream>>>(
+        static_cast<const float*>(a.A), static_cast<const float*>(a.B0),
+        static_cast<const float*>(a.B1), static_cast<float*>(a.out), a.K, a.n_cols,
+        a.tile_expert, a.tile_row0, a.offsets, a.num_mtiles);
+  else
+    gemm_simt_kernel<false><<<grid, 256, 0, stream>>>(
+        static_cast<const float*>(a.A), static_cast<const float*>(a.B0), nullptr,
+        static_cast<float*>(a.out), a.K, a.n_cols, a.tile_expert, a.tile_row0, a.offsets,
+        a.num_mtiles);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

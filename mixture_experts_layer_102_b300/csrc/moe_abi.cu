@@ -1,0 +1,390 @@
+// C-ABI entry points of the MoE forward library (declared in include/moe.h):
+// argument checks, the workspace plan and the launch sequence. Every step of the
+// layer runs in this library's kernels; the host only validates and enqueues.
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#include "../../include/moe.h"
+#include "internal.h"
+
+namespace moe {
+namespace {
+
+constexpr size_t kAlign = 256;
+constexpr int kStatusBytes = 256;  // the status word lives at workspace offset 0
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+struct Plan {
+  int T, H, N, k, F, dtype;
+  long long C;            // -1: no limit
+  int A;                  // T*k routing slots
+  int A_cap;              // rows of the permuted buffers
+  int ksplit, chunks_per_split;
+  int sel_tpw, n_sel_blocks, nchunks, max_mtiles;
+  size_t elem;
+  size_t off_part, off_psum, off_chunk, off_rank, off_idx, off_w, off_drop, off_counts,
+      off_kept, off_offsets, off_tile_e, off_tile_r, off_nmt, off_aux, off_slot_row,
+      off_row_token, off_xp, off_h, off_ye, total;
+};
+
+int check_cfg(const moe_cfg* c) {
+  if (c == nullptr) return MOE_EINVAL;
+  if (c->dtype != MOE_F32 && c->dtype != MOE_BF16) return MOE_EINVAL;
+  if (c->T < 0 || c->H < 1 || c->N < 1 || c->k < 1 || c->F < 1 || c->k > c->N) return MOE_EINVAL;
+  if (!(c->capacity_factor == c->capacity_factor)) return MOE_EINVAL;  // NaN
+  if (c->N > 256 || c->k > 32 || c->H % 64 != 0 || c->F % 64 != 0) return MOE_EUNSUPPORTED;
+  if ((long long)c->T * c->k > (1ll << 30)) return MOE_EUNSUPPORTED;
+  return MOE_OK;
+}
+
+long long capacity_of(const moe_cfg* c) {
+  if (!(c->capacity_factor > 0.0f)) return -1;
+  const double cap = ceil((double)c->capacity_factor * (double)c->T * (double)c->k / (double)c->N);
+  const double slots = (double)c->T * (double)c->k;
+  return cap >= slots ? (long long)slots : (long long)cap;  // an expert never holds more
+}
+
+Plan make_plan(const moe_cfg* c) {
+  Plan p;
+  memset(&p, 0, sizeof(p));
+  p.T = c->T; p.H = c->H; p.N = c->N; p.k = c->k; p.F = c->F; p.dtype = c->dtype;
+  p.C = capacity_of(c);
+  p.A = c->T * c->k;
+  long long cap_rows = p.A;
+  if (p.C >= 0 && (long long)p.N * p.C < cap_rows) cap_rows = (long long)p.N * p.C;
+  p.A_cap = (int)cap_rows;
+  p.elem = c->dtype == MOE_BF16 ? 2 : 4;
+  // Router split over H: keep about two blocks per SM when T is small.
+  const int nblk = (p.T + ROUTER_TOKENS - 1) / ROUTER_TOKENS;
+  const int nchunk = p.H / ROUTER_KC;
+  int ksplit = nblk > 0 ? (296 + nblk - 1) / nblk : 1;
+  if (ksplit > 16) ksplit = 16;
+  if (ksplit > nchunk) ksplit = nchunk;
+  if (ksplit < 1) ksplit = 1;
+  p.chunks_per_split = (nchunk + ksplit - 1) / ksplit;
+  p.ksplit = (nchunk + p.chunks_per_split - 1) / p.chunks_per_split;
+  p.sel_tpw = p.T >= 4096 ? 8 : 1;
+  p.n_sel_blocks = (p.T + 8 * p.sel_tpw - 1) / (8 * p.sel_tpw);
+  p.nchunks = (p.A + COUNT_CHUNK - 1) / COUNT_CHUNK;
+  p.max_mtiles = (p.A_cap + GEMM_BM - 1) / GEMM_BM + p.N;
+
+  size_t cur = kStatusBytes;
+  auto take = [&](size_t bytes) {
+    const size_t o = cur;
+    cur = align_up(cur + (bytes > 0 ? bytes : 1), kAlign);
+    return o;
+  };
+  const size_t T = p.T, N = p.N, A = p.A, Ac = p.A_cap;
+  p.off_part = take((size_t)p.ksplit * T * N * 4);
+  p.off_psum = take((size_t)p.n_sel_blocks * N * 4);
+  p.off_chunk = take((size_t)p.nchunks * N * 4);
+  p.off_rank = take(A * 4);
+  p.off_idx = take(A * 4);
+  p.off_w = take(A * 4);
+  p.off_drop = take(A);
+  p.off_counts = take(N * 4);
+  p.off_kept = take(N * 4);
+  p.off_offsets = take((N + 1) * 4);
+  p.off_tile_e = take((size_t)p.max_mtiles * 4);
+  p.off_tile_r = take((size_t)p.max_mtiles * 4);
+  p.off_nmt = take(4);
+  p.off_aux = take(4);
+  p.off_slot_row = take(A * 4);
+  p.off_row_token = take(Ac * 4);
+  p.off_xp = take(Ac * p.H * p.elem);
+  p.off_h = take(Ac * p.F * p.elem);
+  p.off_ye = take(Ac * p.H * p.elem);
+  p.total = cur;
+  return p;
+}
+
+int device_check() {
+  static int ok_dev[64] = {0};  // 0 unknown, 1 sm_103, -1 other
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ECUDA;
+  if (dev >= 0 && dev < 64 && ok_dev[dev] != 0) return ok_dev[dev] > 0 ? MOE_OK : MOE_ENODEVICE;
+  int major = 0, minor = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+    return MOE_ECUDA;
+  const bool ok = major == 10 && minor == 3;
+  if (dev >= 0 && dev < 64) ok_dev[dev] = ok ? 1 : -1;
+  return ok ? MOE_OK : MOE_ENODEVICE;
+}
+
+#define MOE_TRY(expr)                                \
+  do {                                               \
+    if ((expr) != cudaSuccess) return MOE_ECUDA;     \
+  } while (0)
+
+struct Outs {
+  int32_t* idx;
+  float* w;
+  float* aux;
+  uint8_t* drop;
+  int32_t* counts;
+  int32_t* kept;
+};
+
+// Shared front half: router, capacity, dispatch. `copy` gathers x into xp.
+int run_route(const Plan& p, const void* x, const void* w_router, const float* bias,
+              const Outs& o, uint8_t* ws, bool copy, cudaStream_t s, cudaEvent_t* ev) {
+  auto rec = [&](int i) {
+    if (ev != nullptr) cudaEventRecord(ev[i], s);
+  };
+  uint32_t* status = reinterpret_cast<uint32_t*>(ws);
+  float* part = reinterpret_cast<float*>(ws + p.off_part);
+  float* psum = reinterpret_cast<float*>(ws + p.off_psum);
+  int32_t* chunk = reinterpret_cast<int32_t*>(ws + p.off_chunk);
+  int32_t* rank = reinterpret_cast<int32_t*>(ws + p.off_rank);
+  rec(0);
+  MOE_TRY(launch_router_logits(p.dtype, x, w_router, part, p.T, p.H, p.N, p.ksplit,
+                               p.chunks_per_split, s));
+  rec(1);
+  MOE_TRY(launch_router_select(part, p.ksplit, bias, p.T, p.N, p.k, p.sel_tpw, o.idx, o.w, psum,
+                               s));
+  rec(2);
+  MOE_TRY(launch_capacity_count(o.idx, p.A, p.N, chunk, rank, status, s));
+  rec(3);
+  ScanArgs sa;
+  sa.chunk_counts = chunk;
+  sa.nchunks = p.nchunks;
+  sa.psum_part = psum;
+  sa.npsum = p.n_sel_blocks;
+  sa.T = p.T; sa.k = p.k; sa.N = p.N;
+  sa.C = p.C;
+  sa.counts = reinterpret_cast<int32_t*>(ws + p.off_counts);
+  sa.kept = reinterpret_cast<int32_t*>(ws + p.off_kept);
+  sa.offsets = reinterpret_cast<int32_t*>(ws + p.off_offsets);
+  sa.tile_expert = reinterpret_cast<int32_t*>(ws + p.off_tile_e);
+  sa.tile_row0 = reinterpret_cast<int32_t*>(ws + p.off_tile_r);
+  sa.num_mtiles = reinterpret_cast<int32_t*>(ws + p.off_nmt);
+  sa.aux = o.aux;
+  sa.user_counts = o.counts;
+  sa.user_kept = o.kept;
+  MOE_TRY(launch_capacity_scan(sa, s));
+  rec(4);
+  DispatchArgs da;
+  da.idx = o.idx;
+  da.slot_rank = rank;
+  da.chunk_base = chunk;
+  da.offsets = sa.offsets;
+  da.C = p.C;
+  da.T = p.T; da.k = p.k; da.N = p.N; da.H = p.H;
+  da.A_cap = p.A_cap;
+  da.x = x;
+  da.xp = ws + p.off_xp;
+  da.drop = o.drop;
+  da.slot_row = reinterpret_cast<int32_t*>(ws + p.off_slot_row);
+  da.row_token = reinterpret_cast<int32_t*>(ws + p.off_row_token);
+  da.status = status;
+  MOE_TRY(launch_dispatch(p.dtype, copy, da, s));
+  rec(5);
+  return MOE_OK;
+}
+
+int run_experts(const Plan& p, const void* w1, const void* w3, const void* w2, void* out,
+                const Outs& o, uint8_t* ws, cudaStream_t s, cudaEvent_t* ev) {
+  auto rec = [&](int i) {
+    if (ev != nullptr) cudaEventRecord(ev[i], s);
+  };
+  uint32_t* status = reinterpret_cast<uint32_t*>(ws);
+  GroupedGemmArgs g;
+  g.A = ws + p.off_xp;
+  g.A_rows = p.A_cap;
+  g.B0 = w1;
+  g.B1 = w3;
+  g.out = ws + p.off_h;
+  g.K = p.H;
+  g.n_cols = p.F;
+  g.N = p.N;
+  g.swiglu = true;
+  g.tile_expert = reinterpret_cast<const int32_t*>(ws + p.off_tile_e);
+  g.tile_row0 = reinterpret_cast<const int32_t*>(ws + p.off_tile_r);
+  g.offsets = reinterpret_cast<const int32_t*>(ws + p.off_offsets);
+  g.num_mtiles = reinterpret_cast<const int32_t*>(ws + p.off_nmt);
+  g.max_mtiles = p.max_mtiles;
+  g.status = status;
+  if (p.dtype == MOE_BF16) MOE_TRY(launch_grouped_gemm_tc(g, s));
+  else MOE_TRY(launch_grouped_gemm_simt(g, s));
+  rec(6);
+  g.A = ws + p.off_h;
+  g.B0 = w2;
+  g.B1 = nullptr;
+  g.out = ws + p.off_ye;
+  g.K = p.F;
+  g.n_cols = p.H;
+  g.swiglu = false;
+  if (p.dtype == MOE_BF16) MOE_TRY(launch_grouped_gemm_tc(g, s));
+  else MOE_TRY(launch_grouped_gemm_simt(g, s));
+  rec(7);
+  MOE_TRY(launch_combine(p.dtype, ws + p.off_ye,
+                         reinterpret_cast<const int32_t*>(ws + p.off_slot_row), o.w, p.T, p.k,
+                         p.H, out, s));
+  rec(8);
+  return MOE_OK;
+}
+
+int check_ws(const Plan& p, void* ws, size_t ws_bytes) {
+  if (ws == nullptr || !aligned(ws, kAlign) || ws_bytes < p.total) return MOE_EWORKSPACE;
+  return MOE_OK;
+}
+
+// T = 0: nothing to route; the aux loss and the counts are zero.
+int empty_batch(const Plan& p, float* aux, int32_t* counts, int32_t* kept, cudaStream_t s,
+                cudaEvent_t* ev) {
+  if (ev != nullptr)
+    for (int i = 0; i <= MOE_NUM_STAGES; ++i) cudaEventRecord(ev[i], s);
+  if (aux != nullptr) MOE_TRY(cudaMemsetAsync(aux, 0, sizeof(float), s));
+  if (counts != nullptr) MOE_TRY(cudaMemsetAsync(counts, 0, p.N * sizeof(int32_t), s));
+  if (kept != nullptr) MOE_TRY(cudaMemsetAsync(kept, 0, p.N * sizeof(int32_t), s));
+  return MOE_OK;
+}
+
+int forward_impl(const moe_cfg* cfg, const void* x, const void* w_router, const float* bias,
+                 const void* w1, const void* w3, const void* w2, void* out, int32_t* topk_idx,
+                 float* topk_w, float* aux_loss, uint8_t* drop_mask, int32_t* expert_counts,
+                 int32_t* kept_counts, void* workspace, size_t workspace_bytes, void* stream,
+                 void* const* stage_events) {
+  int rc = check_cfg(cfg);
+  if (rc != MOE_OK) return rc;
+  if (x == nullptr || w_router == nullptr || w1 == nullptr || w3 == nullptr || w2 == nullptr ||
+      out == nullptr)
+    return MOE_EINVAL;
+  if (!aligned(x, 16) || !aligned(w_router, 16) || !aligned(w1, 16) || !aligned(w3, 16) ||
+      !aligned(w2, 16) || !aligned(out, 16) || !aligned(bias, 4) || !aligned(topk_idx, 4) ||
+      !aligned(topk_w, 4) || !aligned(aux_loss, 4) || !aligned(expert_counts, 4) ||
+      !aligned(kept_counts, 4))
+    return MOE_EALIGN;
+  const Plan p = make_plan(cfg);
+  rc = check_ws(p, workspace, workspace_bytes);
+  if (rc != MOE_OK) return rc;
+  rc = device_check();
+  if (rc != MOE_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaEvent_t* ev = stage_events ? reinterpret_cast<cudaEvent_t*>(const_cast<void**>(stage_events))
+                                 : nullptr;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  if (p.T == 0) return empty_batch(p, aux_loss, expert_counts, kept_counts, s, ev);
+  Outs o;
+  o.idx = topk_idx ? topk_idx : reinterpret_cast<int32_t*>(ws + p.off_idx);
+  o.w = topk_w ? topk_w : reinterpret_cast<float*>(ws + p.off_w);
+  o.aux = aux_loss ? aux_loss : reinterpret_cast<float*>(ws + p.off_aux);
+  o.drop = drop_mask ? drop_mask : ws + p.off_drop;
+  o.counts = expert_counts;
+  o.kept = kept_counts;
+  rc = run_route(p, x, w_router, bias, o, ws, true, s, ev);
+  if (rc != MOE_OK) return rc;
+  return run_experts(p, w1, w3, w2, out, o, ws, s, ev);
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+size_t moe_workspace_size(const moe_cfg* cfg) {
+  if (check_cfg(cfg) != MOE_OK) return 0;
+  return make_plan(cfg).total;
+}
+
+int moe_capacity(const moe_cfg* cfg, int64_t* capacity) {
+  if (capacity == nullptr) return MOE_EINVAL;
+  const int rc = check_cfg(cfg);
+  if (rc != MOE_OK) return rc;
+  *capacity = capacity_of(cfg);
+  return MOE_OK;
+}
+
+int moe_workspace_init(void* workspace, size_t workspace_bytes, void* stream) {
+  if (workspace == nullptr || !aligned(workspace, kAlign) || workspace_bytes < (size_t)kStatusBytes)
+    return MOE_EWORKSPACE;
+  const int rc = device_check();
+  if (rc != MOE_OK) return rc;
+  MOE_TRY(cudaMemsetAsync(workspace, 0, kStatusBytes, static_cast<cudaStream_t>(stream)));
+  return MOE_OK;
+}
+
+int moe_route(const moe_cfg* cfg, const void* x, const void* w_router, const float* router_bias,
+              int32_t* topk_idx, float* topk_w, float* aux_loss, uint8_t* drop_mask,
+              int32_t* expert_counts, int32_t* kept_counts, void* workspace,
+              size_t workspace_bytes, void* stream) {
+  int rc = check_cfg(cfg);
+  if (rc != MOE_OK) return rc;
+  if (x == nullptr || w_router == nullptr || topk_idx == nullptr || topk_w == nullptr ||
+      aux_loss == nullptr || drop_mask == nullptr)
+    return MOE_EINVAL;
+  if (!aligned(x, 16) || !aligned(w_router, 16) || !aligned(router_bias, 4) ||
+      !aligned(topk_idx, 4) || !aligned(topk_w, 4) || !aligned(aux_loss, 4) ||
+      !aligned(expert_counts, 4) || !aligned(kept_counts, 4))
+    return MOE_EALIGN;
+  const Plan p = make_plan(cfg);
+  rc = check_ws(p, workspace, workspace_bytes);
+  if (rc != MOE_OK) return rc;
+  rc = device_check();
+  if (rc != MOE_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  if (p.T == 0) return empty_batch(p, aux_loss, expert_counts, kept_counts, s, nullptr);
+  Outs o{topk_idx, topk_w, aux_loss, drop_mask, expert_counts, kept_counts};
+  return run_route(p, x, w_router, router_bias, o, ws, false, s, nullptr);
+}
+
+int moe_forward(const moe_cfg* cfg, const void* x, const void* w_router, const float* router_bias,
+                const void* w1, const void* w3, const void* w2, void* out, int32_t* topk_idx,
+                float* topk_w, float* aux_loss, uint8_t* drop_mask, int32_t* expert_counts,
+                int32_t* kept_counts, void* workspace, size_t workspace_bytes, void* stream) {
+  return forward_impl(cfg, x, w_router, router_bias, w1, w3, w2, out, topk_idx, topk_w, aux_loss,
+                      drop_mask, expert_counts, kept_counts, workspace, workspace_bytes, stream,
+                      nullptr);
+}
+
+int moe_forward_timed(const moe_cfg* cfg, const void* x, const void* w_router,
+                      const float* router_bias, const void* w1, const void* w3, const void* w2,
+                      void* out, int32_t* topk_idx, float* topk_w, float* aux_loss,
+                      uint8_t* drop_mask, int32_t* expert_counts, int32_t* kept_counts,
+                      void* workspace, size_t workspace_bytes, void* stream,
+                      void* const* stage_events) {
+  return forward_impl(cfg, x, w_router, router_bias, w1, w3, w2, out, topk_idx, topk_w, aux_loss,
+                      drop_mask, expert_counts, kept_counts, workspace, workspace_bytes, stream,
+                      stage_events);
+}
+
+int moe_get_status(void* workspace, size_t workspace_bytes, void* stream, uint32_t* bits) {
+  if (workspace == nullptr || !aligned(workspace, kAlign) || workspace_bytes < (size_t)kStatusBytes)
+    return MOE_EWORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint32_t word = 0;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ECUDA;
+  if (cudaMemcpy(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return MOE_ECUDA;
+  if (bits != nullptr) *bits = word;
+  if (word != 0) {
+    if (cudaMemset(workspace, 0, sizeof(word)) != cudaSuccess) return MOE_ECUDA;
+    return MOE_EDEVICE;
+  }
+  return MOE_OK;
+}
+
+const char* moe_strerror(int status) {
+  switch (status) {
+    case MOE_OK: return "ok";
+    case MOE_EINVAL: return "invalid argument";
+    case MOE_EUNSUPPORTED: return "layer shape outside the supported range";
+    case MOE_EWORKSPACE: return "workspace missing, misaligned or too small";
+    case MOE_EALIGN: return "tensor pointer misaligned";
+    case MOE_ECUDA: return "CUDA runtime error";
+    case MOE_EDEVICE: return "a kernel reported a device-side failure";
+    case MOE_ENODEVICE: return "current device is not an sm_103 GPU";
+    default: return "unknown status";
+  }
+}
+
+}  // extern "C"

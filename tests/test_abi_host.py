@@ -1,0 +1,139 @@
+"""Host-side checks of the C-ABI library: it loads, exports every function that
+include/moe.h declares, and its pure-host logic (workspace sizing, capacity, argument
+validation) behaves as documented. No call here reaches a CUDA launch: every failing
+argument check returns before the library touches the CUDA API."""
+import ctypes
+import re
+from pathlib import Path
+
+import numpy as np
+import pytest
+
+import oracle as orc
+from mixture_experts_layer_102_b300 import build, configs, moe
+
+ROOT = Path(__file__).resolve().parents[1]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    build.build(quiet=True)
+
+
+def _declared_functions():
+    text = (ROOT / "include" / "moe.h").read_text()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_\w+)\s*\(", text)))
+
+
+def test_library_exports_every_declared_function():
+    names = _declared_functions()
+    assert set(names) == set(moe._SIGNATURES), names
+    lib = moe.library()
+    for name in names:
+        assert getattr(lib, name) is not None
+
+
+def test_strerror_covers_every_status():
+    for code in range(8):
+        assert moe.strerror(code) != "unknown status"
+    assert moe.strerror(99) == "unknown status"
+
+
+@pytest.mark.parametrize("c", configs.NAMED, ids=lambda c: c.name)
+def test_workspace_size_positive_and_linear_in_tokens(c):
+    s1 = moe.workspace_size(moe.cfg_from(c))
+    s2 = moe.workspace_size(moe.cfg_from(c, T=2 * c.T))
+    assert s1 > 0 and s2 > s1
+    elem = 2 if c.dtype == "bf16" else 4
+    # the permuted rows, h and ye dominate: at least T*k*(2H+F) elements when no
+    # capacity limit bounds them
+    if c.capacity_factor is None:
+        assert s1 >= c.T * c.k * (2 * c.H + c.F) * elem
+
+
+def test_workspace_size_zero_for_invalid():
+    lib = moe.library()
+    bad = [moe.make_cfg(64, 100, 8, 2, 256, None, "bf16"),     # H % 64
+           moe.make_cfg(64, 128, 8, 9, 256, None, "bf16"),     # k > N
+           moe.make_cfg(64, 128, 300, 2, 256, None, "bf16"),   # N > 256
+           moe.make_cfg(-1, 128, 8, 2, 256, None, "bf16")]
+    for cfg in bad:
+        assert lib.moe_workspace_size(ctypes.byref(cfg)) == 0
+    assert lib.moe_workspace_size(None) == 0
+
+
+def test_capacity_matches_oracle():
+    rng = np.random.default_rng(0)
+    for c in configs.NAMED:
+        assert moe.capacity(moe.cfg_from(c)) == orc.capacity(c.T, c.k, c.N, c.capacity_factor)
+    for _ in range(500):
+        T = int(rng.integers(1, 50000))
+        N = int(rng.integers(1, 257))
+        k = int(rng.integers(1, min(N, 32) + 1))
+        cf = float(np.float32(rng.uniform(0.01, 3.0)))
+        got = moe.capacity(moe.make_cfg(T, 64, N, k, 64, cf, "bf16"))
+        want = orc.capacity(T, k, N, cf)
+        assert got == min(want, T * k)
+    assert moe.capacity(moe.make_cfg(10, 64, 4, 2, 64, None, "f32")) is None
+
+
+def _args(cfg, **over):
+    """Plausible fake device pointers; the calls below fail validation first."""
+    d = dict(x=0x10000, wr=0x20000, bias=None, w1=0x30000, w3=0x40000, w2=0x50000,
+             out=0x60000, ws=0x100000, ws_bytes=moe.workspace_size(cfg))
+    d.update(over)
+    return d
+
+
+def _forward(cfg, a):
+    return moe.library().moe_forward(ctypes.byref(cfg), a["x"], a["wr"], a["bias"], a["w1"],
+                                     a["w3"], a["w2"], a["out"], None, None, None, None, None,
+                                     None, a["ws"], a["ws_bytes"], None)
+
+
+def test_forward_rejects_bad_arguments_before_any_cuda_call():
+    cfg = moe.cfg_from(configs.BF16_T4096)
+    assert _forward(cfg, _args(cfg, x=None)) == moe.MOE_EINVAL
+    assert _forward(cfg, _args(cfg, w2=None)) == moe.MOE_EINVAL
+    assert _forward(cfg, _args(cfg, out=0x60008)) == moe.MOE_EALIGN
+    assert _forward(cfg, _args(cfg, bias=0x7002)) == moe.MOE_EALIGN
+    assert _forward(cfg, _args(cfg, ws=None)) == moe.MOE_EWORKSPACE
+    assert _forward(cfg, _args(cfg, ws=0x100010)) == moe.MOE_EWORKSPACE
+    a = _args(cfg)
+    a["ws_bytes"] -= 1
+    assert _forward(cfg, a) == moe.MOE_EWORKSPACE
+    bad_h = moe.make_cfg(64, 96, 8, 2, 256, None, "bf16")
+    assert _forward(bad_h, _args(cfg)) == moe.MOE_EUNSUPPORTED
+    bad_k = moe.make_cfg(64, 128, 4, 5, 256, None, "bf16")
+    assert _forward(bad_k, _args(cfg)) == moe.MOE_EINVAL
+    bad_dtype = moe.make_cfg(64, 128, 4, 2, 256, None, "bf16")
+    bad_dtype.dtype = 7
+    assert _forward(bad_dtype, _args(cfg)) == moe.MOE_EINVAL
+
+
+def test_route_requires_its_outputs():
+    cfg = moe.cfg_from(configs.TINY_F32)
+    lib = moe.library()
+    ws_bytes = moe.workspace_size(cfg)
+    rc = lib.moe_route(ctypes.byref(cfg), 0x10000, 0x20000, None, None, 0x30000, 0x40000,
+                       0x50000, None, None, 0x100000, ws_bytes, None)
+    assert rc == moe.MOE_EINVAL
+    rc = lib.moe_route(ctypes.byref(cfg), 0x10000, 0x20000, None, 0x30002, 0x30000, 0x40000,
+                       0x50000, None, None, 0x100000, ws_bytes, None)
+    assert rc == moe.MOE_EALIGN
+
+
+def test_status_and_init_reject_bad_workspace():
+    lib = moe.library()
+    assert lib.moe_workspace_init(None, 1024, None) == moe.MOE_EWORKSPACE
+    assert lib.moe_workspace_init(0x100001, 1024, None) == moe.MOE_EWORKSPACE
+    assert lib.moe_get_status(0x100000, 16, None, None) == moe.MOE_EWORKSPACE
+
+
+def test_binding_checks_shapes_without_a_gpu():
+    import torch
+    cfg = moe.cfg_from(configs.TINY_F32)
+    x = torch.zeros(cfg.T, cfg.H)
+    with pytest.raises(ValueError):
+        moe.route(cfg, x, torch.zeros(cfg.H, cfg.N))   # CPU tensors are refused
