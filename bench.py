@@ -1,0 +1,468 @@
+"""Benchmark of the MoE layer forward on B300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl reference]
+
+One step is one whole forward of the layer (router, top-k and softmax, aux loss,
+capacity, dispatch, both expert GEMMs, combine) on one batch of synthetic input that
+is already resident in HBM. Inputs are larger than L2 (the expert weights) and the L2
+is flushed (a 256 MiB write) between timed steps, outside the timed events. Each step
+is timed on the device with CUDA events recorded by the library between its stages
+(moe_forward_timed), which also gives every kernel's time for the roofline.
+
+Under torchrun (N > 1) every rank holds all experts and runs its own independent
+batch of T tokens (the same weights, activations drawn from a per-rank seed): the
+layer routes every token on its own, so the batches need no exchange. The slowest
+rank's time sets the whole-job throughput (scaling: weak).
+
+`--impl reference` times the fp64 CPU oracle (the only reference that exists for this
+layer) on the host cores, rank 0 only.
+
+Rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from mixture_experts_layer_102_b300 import configs, inputs  # noqa: E402
+
+METRIC = "MoE layer fwd tokens/s; grouped-GEMM TFLOP/s and routing GB/s as % of B300 peak"
+UNIT = "tokens/s"
+DEFAULT_CONFIG = configs.BF16_T4096
+FLUSH_BYTES = 256 << 20
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+STAGES = ["router_logits", "router_select", "capacity_count", "capacity_scan", "dispatch",
+          "gemm1_swiglu", "gemm2", "combine"]
+# launches of this library's kernels per forward (T > 0)
+LAUNCHES_PER_FORWARD = len(STAGES)
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--config", default=DEFAULT_CONFIG.name)
+    ap.add_argument("--impl", default="mine", choices=["mine", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-budget-s", type=float, default=10.0)
+    return ap.parse_args(argv)
+
+
+# ----------------------------------------------------------------------- ranks
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def init_dist(world: int, backend: str):
+    if world > 1:
+        import torch.distributed as dist
+        if not dist.is_initialized():
+            dist.init_process_group(backend=backend)
+
+
+def barrier(world: int, device=None):
+    if world > 1:
+        import torch.distributed as dist
+        if device is not None:
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+def reduce_max(value: float, world: int, device=None) -> float:
+    """Largest value over all ranks (host-side timing reduction, not data path)."""
+    if world == 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device or "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def reduce_sum(value: float, world: int, device=None) -> float:
+    if world == 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device or "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------- accounting
+
+def algorithmic_units(cfg, kept_slots: int) -> dict:
+    """Algorithmic work per launch of each stage: FLOPs for the GEMMs, bytes for the
+    memory-bound kernels (minimum traffic of the operation, not of this code)."""
+    b = 2 if cfg.dtype == "bf16" else 4
+    T, H, N, F, k = cfg.T, cfg.H, cfg.N, cfg.F, cfg.k
+    return {
+        "router_logits": ("hbm", T * H * b + H * N * b),                 # read x and W_r
+        "router_select": ("hbm", T * k * 8),                             # write idx and w
+        "capacity_count": ("hbm", T * k * 4),
+        "capacity_scan": ("hbm", N * 12),
+        "dispatch": ("hbm", T * H * b + kept_slots * H * b),             # read x, write rows
+        "gemm1_swiglu": ("tensor", 4.0 * H * F * kept_slots),            # x W1^T and x W3^T
+        "gemm2": ("tensor", 2.0 * H * F * kept_slots),
+        "combine": ("hbm", kept_slots * H * b + T * H * b),              # read ye, write out
+    }
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def traffic_record(kernel: str, cfg_name: str):
+    """DRAM bytes per launch from a committed ncu capture, if the kernel's source is
+    unchanged since the capture (profiles/traffic.json holds the source hash)."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)[kernel]
+    except (OSError, ValueError, KeyError):
+        return None
+    if rec.get("config") != cfg_name:
+        return None
+    h = hashlib.sha256()
+    for src in rec.get("sources", []):
+        try:
+            with open(os.path.join(ROOT, src), "rb") as f:
+                h.update(f.read())
+        except OSError:
+            return None
+    if h.hexdigest() != rec.get("sha256"):
+        return None
+    return float(rec["bytes_per_launch"])
+
+
+# ----------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.gpu = gpu_index
+        self.out = None
+
+    def start(self):
+        try:
+            self.out = open(os.devnull if False else f"/tmp/moe_clocks_{os.getpid()}.csv", "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.close()
+        rows = []
+        with open(self.out.name) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.out.name)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ----------------------------------------------------------------- CPU oracle
+
+def blas_threads() -> int:
+    """Threads numpy's BLAS uses (all host cores unless limited)."""
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 1) for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except ImportError:
+        pass
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
+        if os.environ.get(var, "").isdigit():
+            return int(os.environ[var])
+    return len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+
+
+def time_oracle(cfg, budget_s: float) -> dict:
+    """The fp64 oracle as it stands, on the host cores: whole forwards of a bounded
+    sub-batch of the workload (the first S tokens as their own batch), repeated until
+    about `budget_s` of CPU work."""
+    import oracle as orc
+    inp = inputs.make_inputs(cfg)
+    x, wr = inp.values("x"), inp.values("w_router")
+    w1, w3, w2 = inp.values("w1"), inp.values("w3"), inp.values("w2")
+
+    def run(S):
+        t0 = time.perf_counter()
+        orc.moe_forward(x[:S], wr, inp.router_bias, w1, w3, w2, cfg.k, cfg.capacity_factor)
+        return time.perf_counter() - t0
+
+    S = min(cfg.T, 256)
+    dt = run(S)
+    if dt * cfg.T / S < budget_s:
+        S = cfg.T
+    else:
+        S = max(1, min(cfg.T, int(S * budget_s / max(dt, 1e-9))))
+    tokens, elapsed, reps = 0, 0.0, 0
+    while elapsed < budget_s or reps == 0:
+        elapsed += run(S)
+        tokens += S
+        reps += 1
+        if elapsed > 3 * budget_s:
+            break
+    threads = blas_threads()
+    return {"value": tokens / elapsed, "unit": UNIT, "cores": int(threads), "kind": "oracle",
+            "sample": f"{reps} x fp64 oracle forward of the first {S} of {cfg.T} tokens "
+                      f"({cfg.name}), {elapsed:.1f} s"}
+
+
+# --------------------------------------------------------------------- GPU arm
+
+def run_gpu_arm(args, cfg):
+    import torch
+    from mixture_experts_layer_102_b300 import moe
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    init_dist(world, "nccl")
+
+    inp = inputs.make_inputs(cfg, rank=rank)
+    dev = moe.to_device(inp, device)
+    c = moe.cfg_from(cfg)
+    ws = moe.make_workspace(c, device)
+    routing = moe.new_routing(c, device)
+    out = torch.empty((cfg.T, cfg.H), dtype=dev.x.dtype, device=device)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    def step(evs=None):
+        moe.forward(c, dev.x, dev.w_router, dev.router_bias, dev.w1, dev.w3, dev.w2,
+                    workspace=ws, out=out, routing=routing, stream=stream, stage_events=evs)
+
+    ev_sets = [moe.make_stage_events(stream) for _ in range(args.steps)]
+    for _ in range(args.warmup):
+        flush.zero_()
+        step(ev_sets[0])
+    torch.cuda.synchronize(device)
+    moe.get_status(ws)
+    kept_slots = int(routing.kept_counts.sum().item())
+
+    sampler = ClockSampler(local)
+    barrier(world, device)
+    torch.cuda.synchronize(device)
+    sampler.start()
+    time.sleep(0.3)  # let the sampler take its first readings
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()
+        step(ev_sets[i])
+    torch.cuda.synchronize(device)
+    wall = time.perf_counter() - wall0
+    barrier(world, device)
+    clocks = sampler.stop()
+    moe.get_status(ws)
+
+    stage_ms = np.zeros((args.steps, len(STAGES)))
+    for i, evs in enumerate(ev_sets):
+        for s in range(len(STAGES)):
+            stage_ms[i, s] = evs[s].elapsed_time(evs[s + 1])
+    step_ms = stage_ms.sum(axis=1)
+    mean_ms = float(step_ms.mean())
+    max_ms = reduce_max(mean_ms, world, device)
+    total_tokens = reduce_sum(cfg.T, world, device)
+
+    # end to end through the public API: pinned host x in, host out back, every step
+    e2e = None
+    if not args.no_e2e:
+        x_host = moe.to_torch(inp.x, cfg.dtype).pin_memory()
+        out_host = torch.empty((cfg.T, cfg.H), dtype=dev.x.dtype).pin_memory()
+        aux_host = torch.empty(1, dtype=torch.float32).pin_memory()
+        x_dev = torch.empty_like(dev.x)
+
+        def e2e_step():
+            x_dev.copy_(x_host, non_blocking=True)
+            moe.forward(c, x_dev, dev.w_router, dev.router_bias, dev.w1, dev.w3, dev.w2,
+                        workspace=ws, out=out, routing=routing, stream=stream)
+            out_host.copy_(out, non_blocking=True)
+            aux_host.copy_(routing.aux_loss, non_blocking=True)
+            stream.synchronize()
+
+        for _ in range(max(3, args.warmup)):
+            e2e_step()
+        n_e2e = min(args.steps, 200)
+        barrier(world, device)
+        t0 = time.perf_counter()
+        for _ in range(n_e2e):
+            e2e_step()
+        e2e_s = (time.perf_counter() - t0) / n_e2e
+        e2e_s = reduce_max(e2e_s, world, device)
+        moe.get_status(ws)
+        b = 2 if cfg.dtype == "bf16" else 4
+        e2e = {"value": total_tokens / e2e_s, "unit": UNIT,
+               "h2d_bytes_per_step": cfg.T * cfg.H * b,
+               "d2h_bytes_per_step": cfg.T * cfg.H * b + 4,
+               "ms_per_step": e2e_s * 1e3, "steps": n_e2e}
+
+    if rank != 0:
+        return None
+
+    peaks, peak_src = load_peaks()
+    units = algorithmic_units(cfg, kept_slots)
+    mean_stage = stage_ms.mean(axis=0)
+    per_kernel = {}
+    for s, name in enumerate(STAGES):
+        bound, amount = units[name]
+        sec = mean_stage[s] / 1e3
+        if bound == "tensor":
+            ach = amount / sec / 1e12
+            peak = peaks["bf16_tflops"]
+            per_kernel[name] = {"ms": round(mean_stage[s], 5), "TFLOP/s": round(ach, 2),
+                                "frac": round(ach / peak, 4)}
+        else:
+            ach = amount / sec / 1e9
+            per_kernel[name] = {"ms": round(mean_stage[s], 5), "GB/s": round(ach, 1),
+                                "frac": round(ach / peaks["hbm_gbs"], 4)}
+    dom = STAGES[int(np.argmax(mean_stage))]
+    bound, amount = units[dom]
+    sec = mean_stage[STAGES.index(dom)] / 1e3
+    traffic = traffic_record(dom, cfg.name)
+    if bound == "tensor":
+        ach, peak, unit = amount / sec / 1e12, peaks["bf16_tflops"], "TFLOP/s"
+    else:
+        ach, peak, unit = amount / sec / 1e9, peaks["hbm_gbs"], "GB/s"
+    roofline = {"kernel": dom, "bound": bound, "achieved": round(ach, 2), "peak": peak,
+                "unit": unit, "frac": round(ach / peak, 4), "traffic": traffic,
+                "peak_source": f"{peak_src} ({'bf16 burst' if bound == 'tensor' else 'HBM copy'})",
+                "algorithmic_per_launch": amount}
+    gemm_flops = units["gemm1_swiglu"][1] + units["gemm2"][1]
+    gemm_sec = (mean_stage[STAGES.index("gemm1_swiglu")] + mean_stage[STAGES.index("gemm2")]) / 1e3
+    result = {
+        "metric": METRIC, "value": round(total_tokens / (max_ms / 1e3), 1), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(max_ms, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": cfg.dtype, "data": "synthetic (seeded, random-init weights)",
+        "config": {"workload": cfg.name, "T": cfg.T, "H": cfg.H, "N": cfg.N, "k": cfg.k,
+                   "F": cfg.F, "capacity_factor": cfg.capacity_factor,
+                   "kept_slots": kept_slots, "global_tokens": int(total_tokens),
+                   "parallelism": f"dp{world} (independent batches, no collective)",
+                   "l2": "flushed between steps (256 MiB write); weights exceed L2"},
+        "grouped_gemm": {"TFLOP/s": round(gemm_flops / gemm_sec / 1e12, 2),
+                         "frac": round(gemm_flops / gemm_sec / 1e12 / peaks["bf16_tflops"], 4)},
+        "kernels": per_kernel,
+        "roofline": roofline,
+        "gpu_launches": LAUNCHES_PER_FORWARD * args.steps,
+        "clocks": clocks,
+        "wall_s_timed_region": round(wall, 3),
+        "e2e": e2e,
+    }
+    return result
+
+
+def run_reference_arm(args, cfg):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return None
+    import oracle as orc
+    inp = inputs.make_inputs(cfg)
+    x, wr = inp.values("x"), inp.values("w_router")
+    w1, w3, w2 = inp.values("w1"), inp.values("w3"), inp.values("w2")
+
+    def run(S):
+        t0 = time.perf_counter()
+        orc.moe_forward(x[:S], wr, inp.router_bias, w1, w3, w2, cfg.k, cfg.capacity_factor)
+        return time.perf_counter() - t0
+
+    # size one step so that warmup + steps take about two minutes in total
+    per_step_s = 120.0 / max(1, args.steps + args.warmup)
+    S = min(cfg.T, 64)
+    dt = run(S)
+    S = max(1, min(cfg.T, int(S * per_step_s / max(dt, 1e-9))))
+    for _ in range(args.warmup):
+        run(S)
+    total = 0.0
+    for _ in range(args.steps):
+        total += run(S)
+    ms = total / args.steps * 1e3
+    value = S / (ms / 1e3)
+    threads = blas_threads()
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": UNIT,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded, random-init weights)",
+            "config": {"workload": cfg.name, "T": cfg.T, "H": cfg.H, "N": cfg.N, "k": cfg.k,
+                       "F": cfg.F, "capacity_factor": cfg.capacity_factor},
+            "cpu_baseline": {"value": round(value, 2), "unit": UNIT, "cores": int(threads),
+                             "kind": "oracle",
+                             "sample": f"each step: fp64 oracle forward of the first {S} of "
+                                       f"{cfg.T} tokens as their own batch"},
+            "e2e": {"value": round(value, 2), "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    cfg = configs.get(args.config)
+    rank, world, _ = dist_env()
+    if args.impl == "reference":
+        res = run_reference_arm(args, cfg)
+    else:
+        res = run_gpu_arm(args, cfg)
+        if res is not None and world == 1 and not args.no_cpu_baseline:
+            res["cpu_baseline"] = time_oracle(cfg, args.cpu_budget_s)
+        elif res is not None:
+            res["cpu_baseline"] = None
+    if res is not None and rank == 0:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        if dist.is_initialized():
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

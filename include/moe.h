@@ -29,8 +29,9 @@
  *    aux_loss [1] float32.
  *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
  *    stream). A return of MOE_OK means the work was enqueued. Arguments are
- *    checked on the host before anything is enqueued; a failed check enqueues
- *    nothing and touches no CUDA API.
+ *    checked on the host before anything is enqueued; a failed argument check
+ *    enqueues nothing and touches no CUDA API (the device check, which asks the
+ *    runtime for the current device's compute capability, comes after them).
  *  - Kernels report device-side failures (a bounded wait that gave up, an index
  *    out of range) by OR-ing bits into a status word inside the workspace;
  *    moe_get_status() reads and clears it.
@@ -108,7 +109,7 @@ int moe_workspace_init(void* workspace, size_t workspace_bytes, void* stream);
  *   expert_counts  slots per expert before capacity (optional, NULL ok)
  *   kept_counts    slots per expert after capacity (optional, NULL ok)
  * router_bias may be NULL (no bias). Required: x, w_router, topk_idx, topk_w,
- * aux_loss, drop_mask, workspace.
+ * aux_loss, drop_mask, workspace; with T = 0 the [T,...] pointers may be NULL.
  */
 int moe_route(const moe_cfg* cfg, const void* x, const void* w_router,
               const float* router_bias, int32_t* topk_idx, float* topk_w,
@@ -123,7 +124,8 @@ int moe_route(const moe_cfg* cfg, const void* x, const void* w_router,
  * (cf-1.com/news/5914943 section 2.1). Dropped slots contribute 0 and the kept
  * slots keep their weights; the residual is NOT added (the caller adds x), so a
  * token whose every slot was dropped gets out = 0. Required: x, w_router, w1, w3,
- * w2, out, workspace. Optional (NULL ok): router_bias and the routing outputs.
+ * w2, out, workspace (x and out may be NULL when T = 0). Optional (NULL ok):
+ * router_bias and the routing outputs.
  */
 int moe_forward(const moe_cfg* cfg, const void* x, const void* w_router,
                 const float* router_bias, const void* w1, const void* w3,

@@ -60,9 +60,9 @@ capacity_count_kernel(const int32_t* __restrict__ idx, int A, int N,
 // One block of 1024 threads. G = 1024 / pow2ceil(N) threads share an expert column.
 __global__ void __launch_bounds__(1024) capacity_scan_kernel(ScanArgs a) {
   __shared__ int32_t ipart[1024];
-  __shared__ double dpart[1024];
+  __shared__ float fpart[1024];
   __shared__ int32_t s_counts[256], s_kept[256], s_off[257], s_tile0[257];
-  __shared__ double s_psum[256];
+  __shared__ float s_psum[256];
   const int tid = threadIdx.x;
   const int N = a.N;
   int np2 = 1;
@@ -75,22 +75,24 @@ __global__ void __launch_bounds__(1024) capacity_scan_kernel(ScanArgs a) {
   const int Rp = (a.npsum + G - 1) / G;
   const int p0 = min(a.npsum, g * Rp), p1 = min(a.npsum, p0 + Rp);
   int isum = 0;
-  double dsum = 0.0;
+  float fsum = 0.f;
   if (col < N) {
+#pragma unroll 4
     for (int r = r0; r < r1; ++r) isum += a.chunk_counts[(size_t)r * N + col];
-    for (int r = p0; r < p1; ++r) dsum += (double)a.psum_part[(size_t)r * N + col];
+#pragma unroll 4
+    for (int r = p0; r < p1; ++r) fsum += a.psum_part[(size_t)r * N + col];
   }
   ipart[tid] = isum;
-  dpart[tid] = dsum;
+  fpart[tid] = fsum;
   __syncthreads();
   if (col < N && g == 0) {
     int run = 0;
-    double p = 0.0;
+    float p = 0.f;
     for (int q = 0; q < G; ++q) {
       const int v = ipart[tid + q];
       ipart[tid + q] = run;
       run += v;
-      p += dpart[tid + q];
+      p += fpart[tid + q];
     }
     const int kept = (a.C < 0 || (long long)run <= a.C) ? run : (int)a.C;
     s_counts[col] = run;
@@ -112,22 +114,23 @@ __global__ void __launch_bounds__(1024) capacity_scan_kernel(ScanArgs a) {
   }
   if (tid == 0) {
     int off = 0, tiles = 0;
-    double fp = 0.0;
+    float fp = 0.f;
     for (int e = 0; e < N; ++e) {
       s_off[e] = off;
       s_tile0[e] = tiles;
       a.offsets[e] = off;
       off += s_kept[e];
       tiles += (s_kept[e] + GEMM_BM - 1) / GEMM_BM;
-      fp += (double)s_counts[e] * s_psum[e];
+      fp = fmaf((float)s_counts[e], s_psum[e], fp);
     }
     s_off[N] = off;
     s_tile0[N] = tiles;
     a.offsets[N] = off;
     *a.num_mtiles = tiles;
     // aux = N * sum_e (counts_e / (T*k)) * (Psum_e / T)
-    const double Td = (double)a.T;
-    *a.aux = a.T > 0 ? (float)((double)N * fp / (Td * (double)a.k) / Td) : 0.f;
+    // (counts <= T*k and sum_e P_e = T keep every term well inside fp32 range)
+    const float Tf = (float)a.T;
+    *a.aux = a.T > 0 ? (float)N * (fp / (Tf * (float)a.k)) / Tf : 0.f;
   }
   __syncthreads();
   const int total = s_tile0[N];

@@ -68,7 +68,8 @@ Plan make_plan(const moe_cfg* c) {
   if (ksplit < 1) ksplit = 1;
   p.chunks_per_split = (nchunk + ksplit - 1) / ksplit;
   p.ksplit = (nchunk + p.chunks_per_split - 1) / p.chunks_per_split;
-  p.sel_tpw = p.T >= 4096 ? 8 : 1;
+  // router select: one warp per token at a time; enough 8-warp blocks to fill the GPU
+  p.sel_tpw = p.T / 2400 > 1 ? p.T / 2400 : 1;
   p.n_sel_blocks = (p.T + 8 * p.sel_tpw - 1) / (8 * p.sel_tpw);
   p.nchunks = (p.A + COUNT_CHUNK - 1) / COUNT_CHUNK;
   p.max_mtiles = (p.A_cap + GEMM_BM - 1) / GEMM_BM + p.N;
@@ -253,8 +254,9 @@ int forward_impl(const moe_cfg* cfg, const void* x, const void* w_router, const 
                  void* const* stage_events) {
   int rc = check_cfg(cfg);
   if (rc != MOE_OK) return rc;
-  if (x == nullptr || w_router == nullptr || w1 == nullptr || w3 == nullptr || w2 == nullptr ||
-      out == nullptr)
+  // x and out hold T rows: with T = 0 they may be NULL (an empty tensor's address).
+  if (w_router == nullptr || w1 == nullptr || w3 == nullptr || w2 == nullptr ||
+      (cfg->T > 0 && (x == nullptr || out == nullptr)))
     return MOE_EINVAL;
   if (!aligned(x, 16) || !aligned(w_router, 16) || !aligned(w1, 16) || !aligned(w3, 16) ||
       !aligned(w2, 16) || !aligned(out, 16) || !aligned(bias, 4) || !aligned(topk_idx, 4) ||
@@ -318,8 +320,9 @@ int moe_route(const moe_cfg* cfg, const void* x, const void* w_router, const flo
               size_t workspace_bytes, void* stream) {
   int rc = check_cfg(cfg);
   if (rc != MOE_OK) return rc;
-  if (x == nullptr || w_router == nullptr || topk_idx == nullptr || topk_w == nullptr ||
-      aux_loss == nullptr || drop_mask == nullptr)
+  if (w_router == nullptr || aux_loss == nullptr ||
+      (cfg->T > 0 && (x == nullptr || topk_idx == nullptr || topk_w == nullptr ||
+                      drop_mask == nullptr)))
     return MOE_EINVAL;
   if (!aligned(x, 16) || !aligned(w_router, 16) || !aligned(router_bias, 4) ||
       !aligned(topk_idx, 4) || !aligned(topk_w, 4) || !aligned(aux_loss, 4) ||

@@ -1,0 +1,77 @@
+"""Multi-rank host logic of the benchmark on CPU (gloo, world size 2): the timing
+reductions over ranks, the per-rank independent batches, and the reference arm's
+rank-0-only rule. No GPU is involved."""
+import io
+import json
+import os
+import socket
+import sys
+from contextlib import redirect_stdout
+
+import numpy as np
+import pytest
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    sys.path.insert(0, ROOT)
+    import torch.distributed as dist
+
+    import bench
+    from mixture_experts_layer_102_b300 import configs, inputs
+    bench.init_dist(world, "gloo")
+    mx = bench.reduce_max(1.5 + rank, world)
+    sm = bench.reduce_sum(100 * (rank + 1), world)
+    cfg = configs.TINY_F32
+    inp = inputs.make_inputs(cfg, rank=rank)
+    buf = io.StringIO()
+    with redirect_stdout(buf):
+        bench.main(["--impl", "reference", "--config", "tiny", "--steps", "2", "--warmup", "1"])
+    q.put((rank, mx, sm, inp.x.sum(), inp.w1.sum(), buf.getvalue()))
+    if dist.is_initialized():   # bench.main tears the group down itself
+        dist.destroy_process_group()
+
+
+def test_two_gloo_ranks():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = sorted([q.get(timeout=300) for _ in procs])
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    (_, mx0, sm0, x0, w0, out0), (_, mx1, sm1, x1, w1, out1) = res
+    assert mx0 == mx1 == 2.5
+    assert sm0 == sm1 == 300.0
+    assert x0 != x1          # independent batches per rank
+    assert w0 == w1          # the same experts on every rank
+    line = json.loads(out0.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["n_gpus"] == 2 and line["value"] > 0
+    assert line["cpu_baseline"]["kind"] == "oracle"
+    assert out1.strip() == ""  # only rank 0 prints
+
+
+def test_algorithmic_units_match_hand_counts():
+    sys.path.insert(0, ROOT)
+    import bench
+    from mixture_experts_layer_102_b300 import configs
+    c = configs.BF16_T4096
+    u = bench.algorithmic_units(c, kept_slots=8192)
+    assert u["gemm1_swiglu"] == ("tensor", 4.0 * 1024 * 2816 * 8192)
+    assert u["gemm2"] == ("tensor", 2.0 * 1024 * 2816 * 8192)
+    # 6*H*F per kept slot in total: 141.7 GFLOP for 8192 kept slots
+    assert abs(u["gemm1_swiglu"][1] + u["gemm2"][1] - 141.7e9) < 0.1e9
+    assert u["combine"] == ("hbm", 8192 * 1024 * 2 + 4096 * 1024 * 2)
