@@ -11,7 +11,7 @@ namespace moe {
 constexpr int ROUTER_TOKENS = 64;      // tokens per router-logits block
 constexpr int ROUTER_KC = 32;          // hidden columns per router k-chunk
 constexpr int COUNT_CHUNK = 1024;      // routing slots per capacity-count block
-constexpr int GEMM_BM = 128;           // rows per expert GEMM tile
+constexpr int GEMM_BM = 256;           // rows per expert GEMM tile (one CTA pair)
 
 // ---------------------------------------------------------------- router
 // Partial logits part[split][t][e] = sum over this split's hidden columns of
