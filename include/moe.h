@@ -157,6 +157,32 @@ int moe_forward_timed(const moe_cfg* cfg, const void* x, const void* w_router,
 int moe_get_status(void* workspace, size_t workspace_bytes, void* stream,
                    uint32_t* bits);
 
+/*
+ * Routing without a caller-provided workspace, for callers that cannot allocate
+ * device memory: plugin hosts and serving runtimes that plan every device buffer
+ * up front and forbid a kernel library from calling cudaMalloc (an allocation can
+ * synchronise the device, and fails once the runtime has reserved the memory).
+ * The pages have no counterpart of this call; it computes exactly what moe_route
+ * computes, with the same arguments minus the workspace.
+ *
+ * Its scratch is a static device array of MOE_STATIC_SCRATCH_BYTES inside this
+ * library, which every GPU that loads the library holds until the process exits.
+ * The call allocates nothing. It returns MOE_EUNSUPPORTED when the layer's routing
+ * scratch does not fit that array (roughly: ksplit*T*N*4 partial logits plus about
+ * 16*T*k bytes; every named workload here fits). The first call on a device looks
+ * up the array's device address (cudaGetSymbolAddress) with that device current;
+ * make that first call before any stream capture. All calls share the array and it
+ * keeps the last call's contents: calls that overlap on the GPU (other streams,
+ * other threads) race and must be serialised by the caller. Device-side status bits
+ * are cleared at the start of each call and are not reported.
+ */
+#define MOE_STATIC_SCRATCH_BYTES ((size_t)16 << 20)
+
+int moe_route_static(const moe_cfg* cfg, const void* x, const void* w_router,
+                     const float* router_bias, int32_t* topk_idx, float* topk_w,
+                     float* aux_loss, uint8_t* drop_mask, int32_t* expert_counts,
+                     int32_t* kept_counts, void* stream);
+
 /* Static description of a status code. */
 const char* moe_strerror(int status);
 

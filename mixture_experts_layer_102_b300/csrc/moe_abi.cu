@@ -285,6 +285,29 @@ int forward_impl(const moe_cfg* cfg, const void* x, const void* w_router, const 
   return run_experts(p, w1, w3, w2, out, o, ws, s, ev);
 }
 
+// Routing scratch for callers that cannot allocate device memory (see
+// moe_route_static). Every GPU that loads this library holds this array until the
+// process exits; all calls share it.
+constexpr size_t kStaticScratchBytes = MOE_STATIC_SCRATCH_BYTES;
+static __device__ __align__(256) uint8_t g_route_scratch[kStaticScratchBytes];
+
+// Device address of g_route_scratch on the current device. In host code the
+// array's name is only a host-side stand-in, so the address is looked up once per
+// device (with that device current) and cached.
+int static_scratch(uint8_t** out) {
+  static void* addr[64] = {nullptr};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ECUDA;
+  if (addr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_route_scratch) != cudaSuccess || p == nullptr)
+      return MOE_ECUDA;
+    addr[dev] = p;
+  }
+  *out = static_cast<uint8_t*>(addr[dev]);
+  return MOE_OK;
+}
+
 }  // namespace
 }  // namespace moe
 
@@ -335,6 +358,37 @@ int moe_route(const moe_cfg* cfg, const void* x, const void* w_router, const flo
   if (rc != MOE_OK) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
+  if (p.T == 0) return empty_batch(p, aux_loss, expert_counts, kept_counts, s, nullptr);
+  Outs o{topk_idx, topk_w, aux_loss, drop_mask, expert_counts, kept_counts};
+  return run_route(p, x, w_router, router_bias, o, ws, false, s, nullptr);
+}
+
+int moe_route_static(const moe_cfg* cfg, const void* x, const void* w_router,
+                     const float* router_bias, int32_t* topk_idx, float* topk_w, float* aux_loss,
+                     uint8_t* drop_mask, int32_t* expert_counts, int32_t* kept_counts,
+                     void* stream) {
+  int rc = check_cfg(cfg);
+  if (rc != MOE_OK) return rc;
+  if (w_router == nullptr || aux_loss == nullptr ||
+      (cfg->T > 0 && (x == nullptr || topk_idx == nullptr || topk_w == nullptr ||
+                      drop_mask == nullptr)))
+    return MOE_EINVAL;
+  if (!aligned(x, 16) || !aligned(w_router, 16) || !aligned(router_bias, 4) ||
+      !aligned(topk_idx, 4) || !aligned(topk_w, 4) || !aligned(aux_loss, 4) ||
+      !aligned(expert_counts, 4) || !aligned(kept_counts, 4))
+    return MOE_EALIGN;
+  const Plan p = make_plan(cfg);
+  // The routing half uses the workspace prefix that ends where the expert buffers
+  // begin; it must fit the static array.
+  if (p.off_xp > kStaticScratchBytes) return MOE_EUNSUPPORTED;
+  rc = device_check();
+  if (rc != MOE_OK) return rc;
+  uint8_t* ws = nullptr;
+  rc = static_scratch(&ws);
+  if (rc != MOE_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // The array keeps the previous call's contents: the status word must start at 0.
+  MOE_TRY(cudaMemsetAsync(ws, 0, kStatusBytes, s));
   if (p.T == 0) return empty_batch(p, aux_loss, expert_counts, kept_counts, s, nullptr);
   Outs o{topk_idx, topk_w, aux_loss, drop_mask, expert_counts, kept_counts};
   return run_route(p, x, w_router, router_bias, o, ws, false, s, nullptr);

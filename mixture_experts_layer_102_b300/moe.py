@@ -35,6 +35,7 @@ _SIGNATURES = {
     "moe_forward": (ctypes.c_int, [_P] + [_P] * 13 + [_P, ctypes.c_size_t, _P]),
     "moe_forward_timed": (ctypes.c_int, [_P] + [_P] * 13 + [_P, ctypes.c_size_t, _P, _P]),
     "moe_get_status": (ctypes.c_int, [_P, ctypes.c_size_t, _P, ctypes.POINTER(ctypes.c_uint32)]),
+    "moe_route_static": (ctypes.c_int, [_P] + [_P] * 9 + [_P]),
     "moe_strerror": (ctypes.c_char_p, [ctypes.c_int]),
 }
 
