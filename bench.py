@@ -42,8 +42,7 @@ UNIT = "tokens/s"
 DEFAULT_CONFIG = configs.BF16_T4096
 FLUSH_BYTES = 256 << 20
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
-STAGES = ["router_logits", "router_select", "capacity_count", "capacity_scan", "dispatch",
-          "gemm1_swiglu", "gemm2", "combine"]
+STAGES = ["router_logits", "route_select", "dispatch", "gemm1_swiglu", "gemm2", "combine"]
 # launches of this library's kernels per forward (T > 0)
 LAUNCHES_PER_FORWARD = len(STAGES)
 
@@ -109,21 +108,29 @@ def reduce_sum(value: float, world: int, device=None) -> float:
 
 # ------------------------------------------------------------------- accounting
 
-def algorithmic_units(cfg, kept_slots: int) -> dict:
-    """Algorithmic work per launch of each stage: FLOPs for the GEMMs, bytes for the
-    memory-bound kernels (minimum traffic of the operation, not of this code)."""
+def algorithmic_units(cfg, kept_slots: int, touched_experts: int) -> dict:
+    """Algorithmic work per launch of each stage: (FLOPs, bytes) of the operation
+    itself, not of this code. GEMM bytes are the weights of the experts that received
+    at least one kept slot plus the activations read and written once."""
     b = 2 if cfg.dtype == "bf16" else 4
     T, H, N, F, k = cfg.T, cfg.H, cfg.N, cfg.F, cfg.k
+    A = kept_slots
     return {
-        "router_logits": ("hbm", T * H * b + H * N * b),                 # read x and W_r
-        "router_select": ("hbm", T * k * 8),                             # write idx and w
-        "capacity_count": ("hbm", T * k * 4),
-        "capacity_scan": ("hbm", N * 12),
-        "dispatch": ("hbm", T * H * b + kept_slots * H * b),             # read x, write rows
-        "gemm1_swiglu": ("tensor", 4.0 * H * F * kept_slots),            # x W1^T and x W3^T
-        "gemm2": ("tensor", 2.0 * H * F * kept_slots),
-        "combine": ("hbm", kept_slots * H * b + T * H * b),              # read ye, write out
+        "router_logits": (2.0 * T * H * N, T * H * b + H * N * b),       # read x and W_r
+        "route_select": (0.0, T * k * 8),                                # write idx and w
+        "dispatch": (0.0, T * H * b + A * H * b),                        # read x, write rows
+        "gemm1_swiglu": (4.0 * H * F * A,                                # x W1^T and x W3^T
+                         touched_experts * 2 * F * H * b + A * H * b + A * F * b),
+        "gemm2": (2.0 * H * F * A, touched_experts * F * H * b + A * F * b + A * H * b),
+        "combine": (0.0, A * H * b + T * H * b),                         # read ye, write out
     }
+
+
+def bound_of(flops: float, nbytes: float, peaks: dict) -> str:
+    """The roofline a kernel sits under: tensor if its intensity is above the ridge
+    of the measured peaks, HBM otherwise."""
+    ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    return "tensor" if nbytes > 0 and flops / nbytes > ridge else "hbm"
 
 
 def load_peaks():
@@ -291,6 +298,7 @@ def run_gpu_arm(args, cfg):
     torch.cuda.synchronize(device)
     moe.get_status(ws)
     kept_slots = int(routing.kept_counts.sum().item())
+    touched = int((routing.kept_counts > 0).sum().item())
 
     sampler = ClockSampler(local)
     barrier(world, device)
@@ -352,34 +360,34 @@ def run_gpu_arm(args, cfg):
         return None
 
     peaks, peak_src = load_peaks()
-    units = algorithmic_units(cfg, kept_slots)
+    units = algorithmic_units(cfg, kept_slots, touched)
     mean_stage = stage_ms.mean(axis=0)
     per_kernel = {}
     for s, name in enumerate(STAGES):
-        bound, amount = units[name]
+        flops, nbytes = units[name]
         sec = mean_stage[s] / 1e3
-        if bound == "tensor":
-            ach = amount / sec / 1e12
-            peak = peaks["bf16_tflops"]
-            per_kernel[name] = {"ms": round(mean_stage[s], 5), "TFLOP/s": round(ach, 2),
-                                "frac": round(ach / peak, 4)}
-        else:
-            ach = amount / sec / 1e9
-            per_kernel[name] = {"ms": round(mean_stage[s], 5), "GB/s": round(ach, 1),
-                                "frac": round(ach / peaks["hbm_gbs"], 4)}
+        bound = bound_of(flops, nbytes, peaks)
+        ent = {"ms": round(mean_stage[s], 5), "bound": bound,
+               "GB/s": round(nbytes / sec / 1e9, 1)}
+        if flops > 0:
+            ent["TFLOP/s"] = round(flops / sec / 1e12, 2)
+        ent["frac"] = round(ent["TFLOP/s"] / peaks["bf16_tflops"] if bound == "tensor"
+                            else ent["GB/s"] / peaks["hbm_gbs"], 4)
+        per_kernel[name] = ent
     dom = STAGES[int(np.argmax(mean_stage))]
-    bound, amount = units[dom]
+    flops, nbytes = units[dom]
     sec = mean_stage[STAGES.index(dom)] / 1e3
+    bound = bound_of(flops, nbytes, peaks)
     traffic = traffic_record(dom, cfg.name)
     if bound == "tensor":
-        ach, peak, unit = amount / sec / 1e12, peaks["bf16_tflops"], "TFLOP/s"
+        ach, peak, unit, amount = flops / sec / 1e12, peaks["bf16_tflops"], "TFLOP/s", flops
     else:
-        ach, peak, unit = amount / sec / 1e9, peaks["hbm_gbs"], "GB/s"
+        ach, peak, unit, amount = nbytes / sec / 1e9, peaks["hbm_gbs"], "GB/s", nbytes
     roofline = {"kernel": dom, "bound": bound, "achieved": round(ach, 2), "peak": peak,
                 "unit": unit, "frac": round(ach / peak, 4), "traffic": traffic,
                 "peak_source": f"{peak_src} ({'bf16 burst' if bound == 'tensor' else 'HBM copy'})",
                 "algorithmic_per_launch": amount}
-    gemm_flops = units["gemm1_swiglu"][1] + units["gemm2"][1]
+    gemm_flops = units["gemm1_swiglu"][0] + units["gemm2"][0]
     gemm_sec = (mean_stage[STAGES.index("gemm1_swiglu")] + mean_stage[STAGES.index("gemm2")]) / 1e3
     result = {
         "metric": METRIC, "value": round(total_tokens / (max_ms / 1e3), 1), "unit": UNIT,
@@ -388,7 +396,8 @@ def run_gpu_arm(args, cfg):
         "vs_baseline": None, "dtype": cfg.dtype, "data": "synthetic (seeded, random-init weights)",
         "config": {"workload": cfg.name, "T": cfg.T, "H": cfg.H, "N": cfg.N, "k": cfg.k,
                    "F": cfg.F, "capacity_factor": cfg.capacity_factor,
-                   "kept_slots": kept_slots, "global_tokens": int(total_tokens),
+                   "kept_slots": kept_slots, "touched_experts": touched,
+                   "global_tokens": int(total_tokens),
                    "parallelism": f"dp{world} (independent batches, no collective)",
                    "l2": "flushed between steps (256 MiB write); weights exceed L2"},
         "grouped_gemm": {"TFLOP/s": round(gemm_flops / gemm_sec / 1e12, 2),

@@ -74,7 +74,7 @@ typedef struct {
 } moe_cfg;
 
 /* Number of stages moe_forward_timed() brackets with events. */
-#define MOE_NUM_STAGES 8
+#define MOE_NUM_STAGES 6
 
 /*
  * Bytes of device workspace moe_route / moe_forward need for `cfg`; 0 if cfg is
@@ -92,8 +92,10 @@ size_t moe_workspace_size(const moe_cfg* cfg);
 int moe_capacity(const moe_cfg* cfg, int64_t* capacity);
 
 /*
- * Zero the workspace's status word (call once after allocating a workspace whose
- * contents are unknown). Asynchronous on `stream`.
+ * Zero the workspace's first 256 bytes: the status word and a completion counter
+ * that the kernels keep at zero between calls. Call once after allocating a
+ * workspace whose contents are unknown (a zero-filled allocation needs no call).
+ * Asynchronous on `stream`.
  */
 int moe_workspace_init(void* workspace, size_t workspace_bytes, void* stream);
 
@@ -137,10 +139,10 @@ int moe_forward(const moe_cfg* cfg, const void* x, const void* w_router,
 /*
  * moe_forward with stage timing: `stage_events` holds MOE_NUM_STAGES+1 cudaEvent_t
  * handles created by the caller; event i is recorded on `stream` before stage i and
- * event MOE_NUM_STAGES after the last stage. Stages: 0 router logits, 1 router
- * top-k/softmax, 2 capacity count, 3 capacity scan and aux, 4 dispatch (permute),
- * 5 expert GEMM1 + SwiGLU, 6 expert GEMM2, 7 gated combine. NULL stage_events
- * behaves as moe_forward.
+ * event MOE_NUM_STAGES after the last stage. Stages: 0 router logits, 1 routing
+ * decisions (softmax, top-k, gate weights, aux loss, capacity ranks and offsets),
+ * 2 dispatch (permute), 3 expert GEMM1 + SwiGLU, 4 expert GEMM2, 5 gated combine.
+ * NULL stage_events behaves as moe_forward.
  */
 int moe_forward_timed(const moe_cfg* cfg, const void* x, const void* w_router,
                       const float* router_bias, const void* w1, const void* w3,

@@ -26,21 +26,41 @@ combine_kernel(const TIo* __restrict__ ye, const int32_t* __restrict__ slot_row,
     wts[warp][lane] = w[(size_t)t * k + lane];
   }
   __syncwarp();
-  const int nvec = H / 8;
-  for (int v = lane; v < nvec; v += 32) {
-    float acc[8];
+  // Groups of 8 elements (one 16-byte bf16 vector); each lane keeps VPL groups in
+  // flight per slot so the loads of a slot overlap.
+  constexpr int VPL = 4;
+  const int ngrp = H / 8;
+  for (int g0 = 0; g0 < ngrp; g0 += 32 * VPL) {
+    float acc[VPL][8];
 #pragma unroll
-    for (int q = 0; q < 8; ++q) acc[q] = 0.f;
+    for (int u = 0; u < VPL; ++u)
+#pragma unroll
+      for (int q = 0; q < 8; ++q) acc[u][q] = 0.f;
     for (int s = 0; s < k; ++s) {
       const int r = rows[warp][s];
       if (r < 0) continue;
       const float ws = wts[warp][s];
-      float val[8];
-      load8(ye + (size_t)r * H + v * 8, val);
+      const TIo* src = ye + (size_t)r * H;
+      float val[VPL][8];
 #pragma unroll
-      for (int q = 0; q < 8; ++q) acc[q] = fmaf(ws, val[q], acc[q]);
+      for (int u = 0; u < VPL; ++u) {
+        const int g = g0 + u * 32 + lane;
+        if (g < ngrp) load8(src + g * 8, val[u]);
+      }
+#pragma unroll
+      for (int u = 0; u < VPL; ++u) {
+        const int g = g0 + u * 32 + lane;
+        if (g < ngrp) {
+#pragma unroll
+          for (int q = 0; q < 8; ++q) acc[u][q] = fmaf(ws, val[u][q], acc[u][q]);
+        }
+      }
     }
-    store8(out + (size_t)t * H + v * 8, acc);
+#pragma unroll
+    for (int u = 0; u < VPL; ++u) {
+      const int g = g0 + u * 32 + lane;
+      if (g < ngrp) store8(out + (size_t)t * H + g * 8, acc[u]);
+    }
   }
 }
 

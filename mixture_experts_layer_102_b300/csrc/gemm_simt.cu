@@ -11,9 +11,8 @@
 namespace moe {
 namespace {
 
-constexpr int BM = 128;      // rows per block; blockIdx.z picks the half of a tile
-constexpr int BN = 64;       // output columns per block
-static_assert(GEMM_BM == 2 * BM, "a tile-table entry covers two blocks");
+constexpr int BM = TILE_ROWS_1;  // 128 rows: one tile of the 128-row table per block
+constexpr int BN = 64;           // output columns per block
 constexpr int BK = 16;
 
 template <bool SWIGLU>
@@ -25,7 +24,7 @@ gemm_simt_kernel(const float* __restrict__ A, const float* __restrict__ B0,
   const int mt = blockIdx.x;
   if (mt >= *num_mtiles) return;
   const int e = tile_expert[mt];
-  const int r0 = tile_row0[mt] + blockIdx.z * BM;
+  const int r0 = tile_row0[mt];
   const int rend = offsets[e + 1];
   const int n0 = blockIdx.y * BN;
   __shared__ float As[BK][BM + 4];
@@ -88,7 +87,7 @@ gemm_simt_kernel(const float* __restrict__ A, const float* __restrict__ B0,
 
 cudaError_t launch_grouped_gemm_simt(const GroupedGemmArgs& a, cudaStream_t stream) {
   if (a.max_mtiles == 0) return cudaSuccess;
-  const dim3 grid(a.max_mtiles, (a.n_cols + BN - 1) / BN, GEMM_BM / BM);
+  const dim3 grid(a.max_mtiles, (a.n_cols + BN - 1) / BN);
   if (a.swiglu)
     gemm_simt_kernel<true><<<grid, 256, 0, stream>>>(
         static_cast<const float*>(a.A), static_cast<const float*>(a.B0),

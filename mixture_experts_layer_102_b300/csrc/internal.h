@@ -10,8 +10,9 @@ namespace moe {
 // Tile and block geometry shared between the host plan and the kernels.
 constexpr int ROUTER_TOKENS = 64;      // tokens per router-logits block
 constexpr int ROUTER_KC = 32;          // hidden columns per router k-chunk
-constexpr int COUNT_CHUNK = 1024;      // routing slots per capacity-count block
-constexpr int GEMM_BM = 256;           // rows per expert GEMM tile (one CTA pair)
+constexpr int SELECT_WARPS = 32;       // warps per routing-decision block
+constexpr int TILE_ROWS_1 = 128;       // rows per expert GEMM tile on one CTA
+constexpr int TILE_ROWS_2 = 256;       // rows per expert GEMM tile on a CTA pair
 
 // ---------------------------------------------------------------- router
 // Partial logits part[split][t][e] = sum over this split's hidden columns of
@@ -20,43 +21,49 @@ cudaError_t launch_router_logits(int dtype, const void* x, const void* w_router,
                                  int T, int H, int N, int ksplit, int chunks_per_split,
                                  cudaStream_t stream);
 
-// Sums the ksplit partials (+ bias), full softmax (per-block sums of P written to
-// psum_part[block][e]), top-k with the lower-id tie rule and the softmax over the
-// selected logits. tokens_per_warp: 1 or 8 (a block is 8 warps).
-cudaError_t launch_router_select(const float* part, int ksplit, const float* bias, int T, int N,
-                                 int k, int tokens_per_warp, int32_t* idx, float* w,
-                                 float* psum_part, cudaStream_t stream);
+// bf16 router logits on tcgen05: W_r is first copied K-major into wrt [N_pad, H]
+// (N_pad = router_tc_npad(N)); partials as above with the split from router_tc_split.
+int router_tc_npad(int N);
+void router_tc_split(int T, int H, int* ksplit, int* kc_per_split);
+cudaError_t launch_router_logits_tc(const void* x, const void* w_router, void* wrt, float* part,
+                                    int T, int H, int N, uint32_t* status, cudaStream_t stream);
 
-// ---------------------------------------------------------------- capacity
-// For each block of COUNT_CHUNK consecutive slots (slot j = t*k + s): the per-expert
-// slot counts of the block and each slot's rank among the block's earlier slots of
-// the same expert.
-cudaError_t launch_capacity_count(const int32_t* idx, int A, int N, int32_t* chunk_counts,
-                                  int32_t* slot_rank, uint32_t* status, cudaStream_t stream);
-
-struct ScanArgs {
-  int32_t* chunk_counts;        // [nchunks][N] in: counts, out: exclusive bases
-  int nchunks;
-  const float* psum_part;       // [npsum][N]
-  int npsum;
-  int T, k, N;
+// ---------------------------------------------------------------- routing decisions
+struct SelectArgs {
+  const float* part;            // [ksplit][T][N] partial logits
+  int ksplit;
+  const float* bias;            // [N] or null
+  int T, N, k;
+  int tpw;                      // tokens per warp; a block is SELECT_WARPS warps
+  int32_t* idx;                 // [T*k] top-k experts
+  float* w;                     // [T*k] gate weights
+  int32_t* slot_rank;           // [T*k] rank among the block's slots of the expert
+  int32_t* blk_counts;          // [nblk][N] counts, then exclusive per-expert bases
+  float* blk_psum;              // [nblk][N] sums of P
+  unsigned* done;               // completion counter, zero between calls
   long long C;                  // capacity, < 0 for no limit
   int32_t* counts;              // [N] slots per expert before capacity
   int32_t* kept;                // [N] after capacity
   int32_t* offsets;             // [N+1] first permuted row of each expert
-  int32_t* tile_expert;         // [max_mtiles] expert of each GEMM row tile
-  int32_t* tile_row0;           // [max_mtiles] first permuted row of each tile
-  int32_t* num_mtiles;          // [1]
+  // GEMM row-tile tables for 128-row tiles [0] and 256-row tiles [1]: expert and
+  // first permuted row of each tile, and the number of tiles
+  int32_t* tile_expert[2];
+  int32_t* tile_row0[2];
+  int32_t* num_mtiles[2];
   float* aux;                   // [1]
   int32_t* user_counts;         // optional copies for the caller
   int32_t* user_kept;
 };
-cudaError_t launch_capacity_scan(const ScanArgs& a, cudaStream_t stream);
+// Softmax, top-k and gate weights, capacity ranks, and (in the block that finishes
+// last) the per-expert scan, offsets, tile tables and aux loss.
+cudaError_t launch_route_select(const SelectArgs& a, int nblk, cudaStream_t stream);
 
+// ---------------------------------------------------------------- dispatch
 struct DispatchArgs {
   const int32_t* idx;           // [T*k]
-  const int32_t* slot_rank;     // [T*k] rank within its count block
-  const int32_t* chunk_base;    // [nchunks][N]
+  const int32_t* slot_rank;     // [T*k] rank within its routing-decision block
+  const int32_t* blk_base;      // [nblk][N] per-expert base of every such block
+  int tokens_per_block;
   const int32_t* offsets;       // [N+1]
   long long C;
   int T, k, N, H;
@@ -79,7 +86,8 @@ struct GroupedGemmArgs {
   void* out;                    // [A_cap, n_cols]
   int K, n_cols, N;
   bool swiglu;                  // out = silu(A B0^T) * (A B1^T), else A B0^T
-  const int32_t* tile_expert;
+  bool pair;                    // 256-row tiles on CTA pairs (else 128-row tiles)
+  const int32_t* tile_expert;   // the table that matches the tile shape
   const int32_t* tile_row0;
   const int32_t* offsets;
   const int32_t* num_mtiles;

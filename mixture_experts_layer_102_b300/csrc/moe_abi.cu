@@ -13,7 +13,11 @@ namespace moe {
 namespace {
 
 constexpr size_t kAlign = 256;
-constexpr int kStatusBytes = 256;  // the status word lives at workspace offset 0
+// The workspace starts with 256 bytes that must be zero before the first call
+// (moe_workspace_init): the status word at offset 0 and the routing-decision kernel's
+// completion counter at offset 4, which that kernel returns to zero itself.
+constexpr int kStatusBytes = 256;
+constexpr size_t kDoneOffset = 4;
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
@@ -25,10 +29,12 @@ struct Plan {
   int A;                  // T*k routing slots
   int A_cap;              // rows of the permuted buffers
   int ksplit, chunks_per_split;
-  int sel_tpw, n_sel_blocks, nchunks, max_mtiles;
+  int sel_tpw, n_sel_blocks;
+  int max_mtiles[2];      // row tiles of 128 and of 256 rows, upper bounds
+  bool pair;              // expert GEMMs on 256-row tiles (CTA pairs)
   size_t elem;
-  size_t off_part, off_psum, off_chunk, off_rank, off_idx, off_w, off_drop, off_counts,
-      off_kept, off_offsets, off_tile_e, off_tile_r, off_nmt, off_aux, off_slot_row,
+  size_t off_wrt, off_part, off_psum, off_blk, off_rank, off_idx, off_w, off_drop, off_counts,
+      off_kept, off_offsets, off_tile_e[2], off_tile_r[2], off_nmt, off_aux, off_slot_row,
       off_row_token, off_xp, off_h, off_ye, total;
 };
 
@@ -68,11 +74,21 @@ Plan make_plan(const moe_cfg* c) {
   if (ksplit < 1) ksplit = 1;
   p.chunks_per_split = (nchunk + ksplit - 1) / ksplit;
   p.ksplit = (nchunk + p.chunks_per_split - 1) / p.chunks_per_split;
+  if (p.dtype == MOE_BF16) {  // the tensor-core router splits K its own way
+    int kcps = 0;
+    router_tc_split(p.T, p.H, &p.ksplit, &kcps);
+  }
   // router select: one warp per token at a time; enough 8-warp blocks to fill the GPU
-  p.sel_tpw = p.T / 2400 > 1 ? p.T / 2400 : 1;
-  p.n_sel_blocks = (p.T + 8 * p.sel_tpw - 1) / (8 * p.sel_tpw);
-  p.nchunks = (p.A + COUNT_CHUNK - 1) / COUNT_CHUNK;
-  p.max_mtiles = (p.A_cap + GEMM_BM - 1) / GEMM_BM + p.N;
+  // routing decisions: one token per warp at a time; about 600 blocks at most, so
+  // the last block's scan over the blocks stays short
+  p.sel_tpw = p.T / (SELECT_WARPS * 600) > 1 ? p.T / (SELECT_WARPS * 600) : 1;
+  p.n_sel_blocks = (p.T + SELECT_WARPS * p.sel_tpw - 1) / (SELECT_WARPS * p.sel_tpw);
+  p.max_mtiles[0] = (p.A_cap + TILE_ROWS_1 - 1) / TILE_ROWS_1 + p.N;
+  p.max_mtiles[1] = (p.A_cap + TILE_ROWS_2 - 1) / TILE_ROWS_2 + p.N;
+  // Expert GEMM tile shape from the expected rows per expert: large groups go to
+  // CTA pairs (less shared-memory traffic per SM), small ones to single CTAs (less
+  // padding of each expert's last tile, more tiles to spread over the SMs).
+  p.pair = (long long)p.T * p.k >= 1024ll * p.N;
 
   size_t cur = kStatusBytes;
   auto take = [&](size_t bytes) {
@@ -81,9 +97,10 @@ Plan make_plan(const moe_cfg* c) {
     return o;
   };
   const size_t T = p.T, N = p.N, A = p.A, Ac = p.A_cap;
+  p.off_wrt = take(p.dtype == MOE_BF16 ? (size_t)router_tc_npad(p.N) * p.H * 2 : 0);
   p.off_part = take((size_t)p.ksplit * T * N * 4);
   p.off_psum = take((size_t)p.n_sel_blocks * N * 4);
-  p.off_chunk = take((size_t)p.nchunks * N * 4);
+  p.off_blk = take((size_t)p.n_sel_blocks * N * 4);
   p.off_rank = take(A * 4);
   p.off_idx = take(A * 4);
   p.off_w = take(A * 4);
@@ -91,9 +108,11 @@ Plan make_plan(const moe_cfg* c) {
   p.off_counts = take(N * 4);
   p.off_kept = take(N * 4);
   p.off_offsets = take((N + 1) * 4);
-  p.off_tile_e = take((size_t)p.max_mtiles * 4);
-  p.off_tile_r = take((size_t)p.max_mtiles * 4);
-  p.off_nmt = take(4);
+  for (int tb = 0; tb < 2; ++tb) {
+    p.off_tile_e[tb] = take((size_t)p.max_mtiles[tb] * 4);
+    p.off_tile_r[tb] = take((size_t)p.max_mtiles[tb] * 4);
+  }
+  p.off_nmt = take(8);
   p.off_aux = take(4);
   p.off_slot_row = take(A * 4);
   p.off_row_token = take(Ac * 4);
@@ -140,40 +159,44 @@ int run_route(const Plan& p, const void* x, const void* w_router, const float* b
   };
   uint32_t* status = reinterpret_cast<uint32_t*>(ws);
   float* part = reinterpret_cast<float*>(ws + p.off_part);
-  float* psum = reinterpret_cast<float*>(ws + p.off_psum);
-  int32_t* chunk = reinterpret_cast<int32_t*>(ws + p.off_chunk);
-  int32_t* rank = reinterpret_cast<int32_t*>(ws + p.off_rank);
   rec(0);
-  MOE_TRY(launch_router_logits(p.dtype, x, w_router, part, p.T, p.H, p.N, p.ksplit,
-                               p.chunks_per_split, s));
+  if (p.dtype == MOE_BF16)
+    MOE_TRY(launch_router_logits_tc(x, w_router, ws + p.off_wrt, part, p.T, p.H, p.N, status, s));
+  else
+    MOE_TRY(launch_router_logits(p.dtype, x, w_router, part, p.T, p.H, p.N, p.ksplit,
+                                 p.chunks_per_split, s));
   rec(1);
-  MOE_TRY(launch_router_select(part, p.ksplit, bias, p.T, p.N, p.k, p.sel_tpw, o.idx, o.w, psum,
-                               s));
-  rec(2);
-  MOE_TRY(launch_capacity_count(o.idx, p.A, p.N, chunk, rank, status, s));
-  rec(3);
-  ScanArgs sa;
-  sa.chunk_counts = chunk;
-  sa.nchunks = p.nchunks;
-  sa.psum_part = psum;
-  sa.npsum = p.n_sel_blocks;
-  sa.T = p.T; sa.k = p.k; sa.N = p.N;
+  SelectArgs sa;
+  sa.part = part;
+  sa.ksplit = p.ksplit;
+  sa.bias = bias;
+  sa.T = p.T; sa.N = p.N; sa.k = p.k;
+  sa.tpw = p.sel_tpw;
+  sa.idx = o.idx;
+  sa.w = o.w;
+  sa.slot_rank = reinterpret_cast<int32_t*>(ws + p.off_rank);
+  sa.blk_counts = reinterpret_cast<int32_t*>(ws + p.off_blk);
+  sa.blk_psum = reinterpret_cast<float*>(ws + p.off_psum);
+  sa.done = reinterpret_cast<unsigned*>(ws + kDoneOffset);
   sa.C = p.C;
   sa.counts = reinterpret_cast<int32_t*>(ws + p.off_counts);
   sa.kept = reinterpret_cast<int32_t*>(ws + p.off_kept);
   sa.offsets = reinterpret_cast<int32_t*>(ws + p.off_offsets);
-  sa.tile_expert = reinterpret_cast<int32_t*>(ws + p.off_tile_e);
-  sa.tile_row0 = reinterpret_cast<int32_t*>(ws + p.off_tile_r);
-  sa.num_mtiles = reinterpret_cast<int32_t*>(ws + p.off_nmt);
+  for (int tb = 0; tb < 2; ++tb) {
+    sa.tile_expert[tb] = reinterpret_cast<int32_t*>(ws + p.off_tile_e[tb]);
+    sa.tile_row0[tb] = reinterpret_cast<int32_t*>(ws + p.off_tile_r[tb]);
+    sa.num_mtiles[tb] = reinterpret_cast<int32_t*>(ws + p.off_nmt) + tb;
+  }
   sa.aux = o.aux;
   sa.user_counts = o.counts;
   sa.user_kept = o.kept;
-  MOE_TRY(launch_capacity_scan(sa, s));
-  rec(4);
+  MOE_TRY(launch_route_select(sa, p.n_sel_blocks, s));
+  rec(2);
   DispatchArgs da;
   da.idx = o.idx;
-  da.slot_rank = rank;
-  da.chunk_base = chunk;
+  da.slot_rank = sa.slot_rank;
+  da.blk_base = sa.blk_counts;
+  da.tokens_per_block = SELECT_WARPS * p.sel_tpw;
   da.offsets = sa.offsets;
   da.C = p.C;
   da.T = p.T; da.k = p.k; da.N = p.N; da.H = p.H;
@@ -185,7 +208,7 @@ int run_route(const Plan& p, const void* x, const void* w_router, const float* b
   da.row_token = reinterpret_cast<int32_t*>(ws + p.off_row_token);
   da.status = status;
   MOE_TRY(launch_dispatch(p.dtype, copy, da, s));
-  rec(5);
+  rec(3);
   return MOE_OK;
 }
 
@@ -205,15 +228,18 @@ int run_experts(const Plan& p, const void* w1, const void* w3, const void* w2, v
   g.n_cols = p.F;
   g.N = p.N;
   g.swiglu = true;
-  g.tile_expert = reinterpret_cast<const int32_t*>(ws + p.off_tile_e);
-  g.tile_row0 = reinterpret_cast<const int32_t*>(ws + p.off_tile_r);
+  // float32 layers run on CUDA cores over the 128-row table
+  const int tb = (p.dtype == MOE_BF16 && p.pair) ? 1 : 0;
+  g.pair = tb == 1;
+  g.tile_expert = reinterpret_cast<const int32_t*>(ws + p.off_tile_e[tb]);
+  g.tile_row0 = reinterpret_cast<const int32_t*>(ws + p.off_tile_r[tb]);
   g.offsets = reinterpret_cast<const int32_t*>(ws + p.off_offsets);
-  g.num_mtiles = reinterpret_cast<const int32_t*>(ws + p.off_nmt);
-  g.max_mtiles = p.max_mtiles;
+  g.num_mtiles = reinterpret_cast<const int32_t*>(ws + p.off_nmt) + tb;
+  g.max_mtiles = p.max_mtiles[tb];
   g.status = status;
   if (p.dtype == MOE_BF16) MOE_TRY(launch_grouped_gemm_tc(g, s));
   else MOE_TRY(launch_grouped_gemm_simt(g, s));
-  rec(6);
+  rec(4);
   g.A = ws + p.off_h;
   g.B0 = w2;
   g.B1 = nullptr;
@@ -223,11 +249,11 @@ int run_experts(const Plan& p, const void* w1, const void* w3, const void* w2, v
   g.swiglu = false;
   if (p.dtype == MOE_BF16) MOE_TRY(launch_grouped_gemm_tc(g, s));
   else MOE_TRY(launch_grouped_gemm_simt(g, s));
-  rec(7);
+  rec(5);
   MOE_TRY(launch_combine(p.dtype, ws + p.off_ye,
                          reinterpret_cast<const int32_t*>(ws + p.off_slot_row), o.w, p.T, p.k,
                          p.H, out, s));
-  rec(8);
+  rec(6);
   return MOE_OK;
 }
 

@@ -1,0 +1,323 @@
+// Routing decisions of the MoE layer in one launch: softmax, top-k and gate weights
+// per token, the load-balancing statistics and aux loss, and the per-expert capacity
+// ranks, offsets and GEMM tile tables.
+//
+//   P = softmax(logits) over all N experts; idx = top-k of the logits (ties to the
+//   lower expert id); w = softmax over the k selected logits
+//     (cf-1.com/news/5914943 section 2.1; hotelren.com/news/3071227 section 4.1;
+//      2kiu.com/news/2885792 section 5.3)
+//   aux = N * sum_e (counts_e / (T*k)) * (sum_t P[t,e] / T), counts before capacity
+//     (cf-1.com/news/5914943 section 2.3)
+//   rank of a slot = number of earlier slots (token order) routed to its expert; the
+//   first C slots of every expert are kept (2kiu.com/news/2885792 section 3.1;
+//   cf-1.com/news/5914943 section 2.3 note)
+//
+// A block is 32 warps; warp w handles `tpw` consecutive tokens, one at a time, and
+// lane l owns experts l, l+32, ... of the current token. Each warp keeps running
+// per-expert counters in shared memory, which give every slot its rank among the
+// block's earlier slots of the same expert (a token picks an expert at most once, so
+// slots of one expert are ordered by token); a prefix over the warps turns them into
+// in-block ranks. No atomics decide positions, so the kept set never depends on
+// scheduling. The partial logits of the split-K router GEMM are summed in a fixed
+// order and every reduction has a fixed shape, so the results are bit-reproducible.
+//
+// The block that finishes last (a device-wide completion counter, no waiting) scans
+// the per-block counts of every expert into per-block bases, and writes the totals,
+// kept = min(count, C), the expert offsets, the GEMM row-tile tables and the aux loss;
+// it then resets the counter for the next call.
+#include <math.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+namespace {
+
+constexpr int WARPS = SELECT_WARPS;  // 32
+constexpr int MAX_TPW = 4;           // tokens per warp whose ranks stay in registers
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// Column scan of the per-block counts by the last block (1024 threads): G threads
+// share an expert column and each walks a contiguous range of block rows.
+__device__ void finish_routing(const SelectArgs& a, int nblk) {
+  __shared__ int32_t ipart[1024];
+  __shared__ float fpart[1024];
+  __shared__ int32_t s_counts[256], s_kept[256], s_off[257], s_tile0[2][257];
+  __shared__ float s_psum[256];
+  const int tid = threadIdx.x;
+  const int N = a.N;
+  int np2 = 1;
+  while (np2 < N) np2 <<= 1;
+  const int G = 1024 / np2;
+  const int col = tid / G, g = tid - col * G;
+  const int R = (nblk + G - 1) / G;
+  const int r0 = min(nblk, g * R), r1 = min(nblk, r0 + R);
+  constexpr int B = 8;  // rows per batch: B loads in flight per thread
+  int isum = 0;
+  float fsum = 0.f;
+  if (col < N) {
+    for (int rb = r0; rb < r1; rb += B) {
+      int iv[B];
+      float fv[B];
+#pragma unroll
+      for (int u = 0; u < B; ++u) {
+        const bool in = rb + u < r1;
+        iv[u] = in ? a.blk_counts[(size_t)(rb + u) * N + col] : 0;
+        fv[u] = in ? a.blk_psum[(size_t)(rb + u) * N + col] : 0.f;
+      }
+#pragma unroll
+      for (int u = 0; u < B; ++u) {
+        isum += iv[u];
+        fsum += fv[u];
+      }
+    }
+  }
+  ipart[tid] = isum;
+  fpart[tid] = fsum;
+  __syncthreads();
+  if (col < N && g == 0) {
+    int run = 0;
+    float p = 0.f;
+    for (int q = 0; q < G; ++q) {
+      const int v = ipart[tid + q];
+      ipart[tid + q] = run;
+      run += v;
+      p += fpart[tid + q];
+    }
+    const int kept = (a.C < 0 || (long long)run <= a.C) ? run : (int)a.C;
+    s_counts[col] = run;
+    s_kept[col] = kept;
+    s_psum[col] = p;
+    a.counts[col] = run;
+    a.kept[col] = kept;
+    if (a.user_counts != nullptr) a.user_counts[col] = run;
+    if (a.user_kept != nullptr) a.user_kept[col] = kept;
+  }
+  __syncthreads();
+  if (col < N) {  // exclusive per-expert base of every block
+    int run = ipart[tid];
+    for (int rb = r0; rb < r1; rb += B) {
+      int iv[B];
+#pragma unroll
+      for (int u = 0; u < B; ++u)
+        iv[u] = rb + u < r1 ? a.blk_counts[(size_t)(rb + u) * N + col] : 0;
+#pragma unroll
+      for (int u = 0; u < B; ++u) {
+        if (rb + u < r1) a.blk_counts[(size_t)(rb + u) * N + col] = run;
+        run += iv[u];
+      }
+    }
+  }
+  if (tid == 0) {
+    int off = 0, tiles1 = 0, tiles2 = 0;
+    float fp = 0.f;
+    for (int e = 0; e < N; ++e) {
+      s_off[e] = off;
+      s_tile0[0][e] = tiles1;
+      s_tile0[1][e] = tiles2;
+      a.offsets[e] = off;
+      off += s_kept[e];
+      tiles1 += (s_kept[e] + TILE_ROWS_1 - 1) / TILE_ROWS_1;
+      tiles2 += (s_kept[e] + TILE_ROWS_2 - 1) / TILE_ROWS_2;
+      fp = fmaf((float)s_counts[e], s_psum[e], fp);
+    }
+    s_off[N] = off;
+    s_tile0[0][N] = tiles1;
+    s_tile0[1][N] = tiles2;
+    a.offsets[N] = off;
+    *a.num_mtiles[0] = tiles1;
+    *a.num_mtiles[1] = tiles2;
+    // aux = N * sum_e (counts_e / (T*k)) * (Psum_e / T); counts <= T*k and
+    // sum_e Psum_e = T keep every term well inside fp32 range
+    const float Tf = (float)a.T;
+    *a.aux = a.T > 0 ? (float)N * (fp / (Tf * (float)a.k)) / Tf : 0.f;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int tb = 0; tb < 2; ++tb) {
+    const int rows = tb == 0 ? TILE_ROWS_1 : TILE_ROWS_2;
+    const int32_t* t0 = s_tile0[tb];
+    const int total = t0[N];
+    for (int i = tid; i < total; i += 1024) {
+      int lo = 0, hi = N - 1;  // last expert with t0[e] <= i
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (t0[mid] <= i) lo = mid; else hi = mid - 1;
+      }
+      a.tile_expert[tb][i] = lo;
+      a.tile_row0[tb][i] = s_off[lo] + (i - t0[lo]) * rows;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(1024) route_select_kernel(SelectArgs a) {
+  extern __shared__ int32_t dyn[];
+  int32_t* cnt = dyn;                                   // [WARPS][N] running counts
+  float* pw = reinterpret_cast<float*>(dyn + WARPS * a.N);  // [WARPS][N] sums of P
+  __shared__ int is_last;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int N = a.N, k = a.k;
+  for (int i = threadIdx.x; i < WARPS * N; i += blockDim.x) {
+    cnt[i] = 0;
+    pw[i] = 0.f;
+  }
+  __syncthreads();
+  const int NI = (N + 31) >> 5;  // experts per lane, <= 8
+  const int tbase = (blockIdx.x * WARPS + warp) * a.tpw;
+  // warp-local rank and expert of this lane's slot for the first MAX_TPW tokens
+  int rank_i[MAX_TPW], exp_i[MAX_TPW];
+#pragma unroll
+  for (int u = 0; u < MAX_TPW; ++u) rank_i[u] = exp_i[u] = 0;
+  for (int i = 0; i < a.tpw; ++i) {
+    const int t = tbase + i;
+    if (t >= a.T) break;
+    float v[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) v[q] = (q < NI && lane + 32 * q < N) ? 0.f : -INFINITY;
+    // sum the split partials in split order; the loads of one split are independent
+    for (int p = 0; p < a.ksplit; ++p) {
+      const float* row = a.part + ((size_t)p * a.T + t) * N;
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        if (q < NI && lane + 32 * q < N) v[q] += row[lane + 32 * q];
+    }
+    if (a.bias != nullptr) {
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        if (q < NI && lane + 32 * q < N) v[q] += a.bias[lane + 32 * q];
+    }
+    // softmax over all N experts
+    float m = -INFINITY;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) m = fmaxf(m, v[q]);
+    m = warp_max(m);
+    float ex[8], sum = 0.f;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const int e = lane + 32 * q;
+      ex[q] = (q < NI && e < N) ? expf(v[q] - m) : 0.f;
+      sum += ex[q];
+    }
+    sum = warp_sum(sum);
+    const float inv = 1.f / sum;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const int e = lane + 32 * q;
+      if (q < NI && e < N) pw[warp * N + e] += ex[q] * inv;
+    }
+    // top-k: k rounds of a warp arg-max on (logit desc, expert id asc)
+    uint32_t taken = 0;
+    float my_l = 0.f, l0 = 0.f;
+    int my_i = 0;
+    for (int s = 0; s < k; ++s) {
+      float bv = -INFINITY;
+      int bi = 0x7fffffff;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const int e = lane + 32 * q;
+        if (q < NI && e < N && !((taken >> q) & 1u) && v[q] > bv) {  // e ascends with q
+          bv = v[q];
+          bi = e;
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+        if (ov > bv || (ov == bv && oi < bi)) {
+          bv = ov;
+          bi = oi;
+        }
+      }
+      if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+      if (s == 0) l0 = bv;
+      if (lane == s) {
+        my_l = bv;
+        my_i = bi;
+      }
+    }
+    // gate weights (softmax over the k selected logits) and warp-local ranks; the k
+    // experts of a token are distinct, so the lanes update distinct counters
+    const float z = (lane < k) ? expf(my_l - l0) : 0.f;
+    const float zs = warp_sum(z);
+    if (lane < k) {
+      const size_t j = (size_t)t * k + lane;
+      a.idx[j] = my_i;
+      a.w[j] = z / zs;
+      const int r = cnt[warp * N + my_i]++;
+      if (i < MAX_TPW) {
+#pragma unroll
+        for (int u = 0; u < MAX_TPW; ++u)
+          if (u == i) {
+            rank_i[u] = r;
+            exp_i[u] = my_i;
+          }
+      } else {
+        a.slot_rank[j] = r;
+      }
+    }
+    __syncwarp();
+  }
+  __syncthreads();
+  // exclusive prefix of the counters over the warps: the block's per-expert offsets
+  for (int e = threadIdx.x; e < N; e += blockDim.x) {
+    int run = 0;
+    float ps = 0.f;
+    for (int w = 0; w < WARPS; ++w) {
+      const int c = cnt[w * N + e];
+      cnt[w * N + e] = run;
+      run += c;
+      ps += pw[w * N + e];
+    }
+    a.blk_counts[(size_t)blockIdx.x * N + e] = run;
+    a.blk_psum[(size_t)blockIdx.x * N + e] = ps;
+  }
+  __syncthreads();
+  for (int i = 0; i < a.tpw; ++i) {  // warp-local ranks -> in-block ranks
+    const int t = tbase + i;
+    if (t >= a.T) break;
+    if (lane < k) {
+      const size_t j = (size_t)t * k + lane;
+      if (i < MAX_TPW) {
+#pragma unroll
+        for (int u = 0; u < MAX_TPW; ++u)  // static indexing keeps the arrays in registers
+          if (u == i) a.slot_rank[j] = rank_i[u] + cnt[warp * N + exp_i[u]];
+      } else {
+        a.slot_rank[j] += cnt[warp * N + a.idx[j]];
+      }
+    }
+  }
+  // The last block to get here finishes the layer-wide statistics.
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) is_last = atomicAdd(a.done, 1u) == gridDim.x - 1;
+  __syncthreads();
+  if (!is_last) return;
+  __threadfence();
+  finish_routing(a, gridDim.x);
+  if (threadIdx.x == 0) *a.done = 0u;  // ready for the next call
+}
+
+}  // namespace
+
+cudaError_t launch_route_select(const SelectArgs& a, int nblk, cudaStream_t stream) {
+  if (a.T == 0) return cudaSuccess;
+  const size_t smem = (size_t)WARPS * a.N * 8;  // counters and P sums of every warp
+  const cudaError_t e = cudaFuncSetAttribute(
+      route_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  route_select_kernel<<<nblk, WARPS * 32, smem, stream>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -4,11 +4,10 @@
 // hotelren.com/news/3071227 section 4.1 TopKRouter; stable tie order from
 // 2kiu.com/news/2885792 section 5.3).
 //
-// Two kernels. router_logits_kernel is a split-K fp32 GEMM [T,H]x[H,N] on CUDA
-// cores: N <= 256 makes it a thin product that is bound by reading x once, and
-// the split over H keeps 2 blocks per SM busy when T is small (decode).
-// router_select_kernel sums the split partials in a fixed order, so the logits are
-// deterministic, then does one token per warp: lane l owns experts l, l+32, ...
+// router_logits_kernel is a split-K fp32 GEMM [T,H]x[H,N] on CUDA cores: N <= 256
+// makes it a thin product that is bound by reading x once, and the split over H keeps
+// 2 blocks per SM busy when T is small (decode). The routing decisions that follow
+// (softmax, top-k, gate weights) are in route_select.cu.
 #include <math.h>
 
 #include "common.cuh"
@@ -96,109 +95,6 @@ router_logits_kernel(const TIn* __restrict__ x, const TIn* __restrict__ wr,
   }
 }
 
-__device__ __forceinline__ float warp_max(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-  return v;
-}
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
-}
-
-// A block is 8 warps; each warp handles `tpw` consecutive tokens in order.
-__global__ void __launch_bounds__(256)
-router_select_kernel(const float* __restrict__ part, int ksplit, const float* __restrict__ bias,
-                     int T, int N, int k, int tpw, int32_t* __restrict__ idx_out,
-                     float* __restrict__ w_out, float* __restrict__ psum_part) {
-  extern __shared__ float psw[];  // [8][N] per-warp sums of P
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int e = lane; e < N; e += 32) psw[warp * N + e] = 0.f;
-  __syncwarp();
-  const int NI = (N + 31) >> 5;  // experts per lane, <= 8
-  const int tbase = (blockIdx.x * 8 + warp) * tpw;
-  for (int i = 0; i < tpw; ++i) {
-    const int t = tbase + i;
-    if (t >= T) break;
-    float v[8];
-#pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      const int e = lane + 32 * q;
-      float s = -INFINITY;
-      if (q < NI && e < N) {
-        s = 0.f;
-        for (int p = 0; p < ksplit; ++p) s += part[((size_t)p * T + t) * N + e];
-        if (bias != nullptr) s += bias[e];
-      }
-      v[q] = s;
-    }
-    // softmax over all N experts
-    float m = -INFINITY;
-#pragma unroll
-    for (int q = 0; q < 8; ++q) m = fmaxf(m, v[q]);
-    m = warp_max(m);
-    float ex[8], sum = 0.f;
-#pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      const int e = lane + 32 * q;
-      ex[q] = (q < NI && e < N) ? expf(v[q] - m) : 0.f;
-      sum += ex[q];
-    }
-    sum = warp_sum(sum);
-    const float inv = 1.f / sum;
-#pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      const int e = lane + 32 * q;
-      if (q < NI && e < N) psw[warp * N + e] += ex[q] * inv;
-    }
-    // top-k: k rounds of a warp arg-max on (logit desc, expert id asc)
-    uint32_t taken = 0;
-    float my_l = 0.f, l0 = 0.f;
-    int my_i = 0;
-    for (int s = 0; s < k; ++s) {
-      float bv = -INFINITY;
-      int bi = 0x7fffffff;
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        const int e = lane + 32 * q;
-        if (q < NI && e < N && !((taken >> q) & 1u) && v[q] > bv) {  // e ascends with q
-          bv = v[q];
-          bi = e;
-        }
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-        if (ov > bv || (ov == bv && oi < bi)) {
-          bv = ov;
-          bi = oi;
-        }
-      }
-      if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-      if (s == 0) l0 = bv;
-      if (lane == s) {
-        my_l = bv;
-        my_i = bi;
-      }
-    }
-    // gate weights: softmax over the k selected logits
-    const float z = (lane < k) ? expf(my_l - l0) : 0.f;
-    const float zs = warp_sum(z);
-    if (lane < k) {
-      idx_out[(size_t)t * k + lane] = my_i;
-      w_out[(size_t)t * k + lane] = z / zs;
-    }
-  }
-  __syncthreads();
-  for (int e = threadIdx.x; e < N; e += 256) {
-    float s = 0.f;
-    for (int w = 0; w < 8; ++w) s += psw[w * N + e];
-    psum_part[(size_t)blockIdx.x * N + e] = s;
-  }
-}
-
 template <typename TIn>
 cudaError_t launch_logits_t(const TIn* x, const TIn* wr, float* part, int T, int H, int N,
                             int ksplit, int cps, cudaStream_t stream) {
@@ -228,17 +124,6 @@ cudaError_t launch_router_logits(int dtype, const void* x, const void* w_router,
                            chunks_per_split, stream);
   return launch_logits_t(static_cast<const float*>(x), static_cast<const float*>(w_router), part,
                          T, H, N, ksplit, chunks_per_split, stream);
-}
-
-cudaError_t launch_router_select(const float* part, int ksplit, const float* bias, int T, int N,
-                                 int k, int tokens_per_warp, int32_t* idx, float* w,
-                                 float* psum_part, cudaStream_t stream) {
-  if (T == 0) return cudaSuccess;
-  const int per_block = 8 * tokens_per_warp;
-  const int blocks = (T + per_block - 1) / per_block;
-  router_select_kernel<<<blocks, 256, 8 * N * sizeof(float), stream>>>(
-      part, ksplit, bias, T, N, k, tokens_per_warp, idx, w, psum_part);
-  return cudaGetLastError();
 }
 
 }  // namespace moe

@@ -21,9 +21,8 @@ LIB_PATH = os.path.join(_HERE, "libmoe_b300.so")
 MOE_OK, MOE_EINVAL, MOE_EUNSUPPORTED, MOE_EWORKSPACE, MOE_EALIGN = 0, 1, 2, 3, 4
 MOE_ECUDA, MOE_EDEVICE, MOE_ENODEVICE = 5, 6, 7
 MOE_F32, MOE_BF16 = 0, 1
-MOE_NUM_STAGES = 8
-STAGE_NAMES = ["router_logits", "router_select", "capacity_count", "capacity_scan",
-               "dispatch", "gemm1_swiglu", "gemm2", "combine"]
+MOE_NUM_STAGES = 6
+STAGE_NAMES = ["router_logits", "route_select", "dispatch", "gemm1_swiglu", "gemm2", "combine"]
 
 # Every function the header declares, with its C signature.
 _P = ctypes.c_void_p

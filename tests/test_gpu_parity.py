@@ -159,6 +159,10 @@ SMALL = [
     MoEConfig("bf16_zipf_drops", 2048, 128, 64, 2, 128, 1.2, "bf16", seed=6, zipf_bias=True),
     MoEConfig("bf16_single_token", 1, 128, 8, 2, 128, 1.25, "bf16", seed=7),
     MoEConfig("f32_ragged", 300, 192, 5, 2, 320, 0.9, "f32", seed=8),
+    # at least 1024 expected rows per expert: 256-row tiles on CTA pairs
+    MoEConfig("bf16_pair_ragged_t3000", 3000, 256, 4, 2, 384, 1.25, "bf16", seed=12),
+    MoEConfig("bf16_pair_edge_h320_f192", 2100, 320, 2, 1, 192, 1.3, "bf16", seed=13),
+    MoEConfig("bf16_pair_drops", 4096, 128, 4, 2, 128, 1.02, "bf16", seed=14, zipf_bias=True),
 ]
 
 

@@ -69,9 +69,17 @@ def test_algorithmic_units_match_hand_counts():
     import bench
     from mixture_experts_layer_102_b300 import configs
     c = configs.BF16_T4096
-    u = bench.algorithmic_units(c, kept_slots=8192)
-    assert u["gemm1_swiglu"] == ("tensor", 4.0 * 1024 * 2816 * 8192)
-    assert u["gemm2"] == ("tensor", 2.0 * 1024 * 2816 * 8192)
+    u = bench.algorithmic_units(c, kept_slots=8192, touched_experts=16)
+    assert u["gemm1_swiglu"][0] == 4.0 * 1024 * 2816 * 8192
+    assert u["gemm2"][0] == 2.0 * 1024 * 2816 * 8192
     # 6*H*F per kept slot in total: 141.7 GFLOP for 8192 kept slots
-    assert abs(u["gemm1_swiglu"][1] + u["gemm2"][1] - 141.7e9) < 0.1e9
-    assert u["combine"] == ("hbm", 8192 * 1024 * 2 + 4096 * 1024 * 2)
+    assert abs(u["gemm1_swiglu"][0] + u["gemm2"][0] - 141.7e9) < 0.1e9
+    # GEMM1 reads W1 and W3 of all 16 experts (184.5 MB) plus xp, and writes h
+    assert u["gemm1_swiglu"][1] == 16 * 2 * 2816 * 1024 * 2 + 8192 * 1024 * 2 + 8192 * 2816 * 2
+    assert u["combine"] == (0.0, 8192 * 1024 * 2 + 4096 * 1024 * 2)
+    peaks = {"bf16_tflops": 1797.5, "hbm_gbs": 6484.3}
+    assert bench.bound_of(*u["gemm1_swiglu"], peaks) == "tensor"
+    assert bench.bound_of(*u["combine"], peaks) == "hbm"
+    d = configs.DECODE_T64  # 128 slots over 75 experts: weight streaming, ~1 FLOP/B
+    ud = bench.algorithmic_units(d, kept_slots=128, touched_experts=75)
+    assert bench.bound_of(*ud["gemm1_swiglu"], peaks) == "hbm"
