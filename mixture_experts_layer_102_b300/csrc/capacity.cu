@@ -20,6 +20,8 @@ __global__ void __launch_bounds__(256) dispatch_kernel(DispatchArgs a) {
   __shared__ int32_t rows[8][32];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * 8 + warp;
+  pdl_wait();  // ranks, bases and offsets come from the routing-decision kernel
+  pdl_trigger();
   if (t >= a.T) return;
   int row = -1;
   if (lane < a.k) {
@@ -77,17 +79,16 @@ __global__ void __launch_bounds__(256) dispatch_kernel(DispatchArgs a) {
 
 }  // namespace
 
-cudaError_t launch_dispatch(int dtype, bool copy, const DispatchArgs& a, cudaStream_t stream) {
+cudaError_t launch_dispatch(int dtype, bool copy, const DispatchArgs& a, cudaStream_t stream,
+                            bool pdl) {
   if (a.T == 0) return cudaSuccess;
-  const int blocks = (a.T + 7) / 8;
-  if (dtype == 1) {
-    if (copy) dispatch_kernel<__nv_bfloat16, true><<<blocks, 256, 0, stream>>>(a);
-    else dispatch_kernel<__nv_bfloat16, false><<<blocks, 256, 0, stream>>>(a);
-  } else {
-    if (copy) dispatch_kernel<float, true><<<blocks, 256, 0, stream>>>(a);
-    else dispatch_kernel<float, false><<<blocks, 256, 0, stream>>>(a);
-  }
-  return cudaGetLastError();
+  const dim3 grid((a.T + 7) / 8), block(256);
+  if (dtype == 1)
+    return copy ? launch_kernel(dispatch_kernel<__nv_bfloat16, true>, grid, block, 0, stream, pdl, a)
+                : launch_kernel(dispatch_kernel<__nv_bfloat16, false>, grid, block, 0, stream, pdl,
+                                a);
+  return copy ? launch_kernel(dispatch_kernel<float, true>, grid, block, 0, stream, pdl, a)
+              : launch_kernel(dispatch_kernel<float, false>, grid, block, 0, stream, pdl, a);
 }
 
 }  // namespace moe

@@ -20,6 +20,8 @@ combine_kernel(const TIo* __restrict__ ye, const int32_t* __restrict__ slot_row,
   __shared__ float wts[8][32];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * 8 + warp;
+  pdl_wait();  // ye comes from the second expert GEMM
+  pdl_trigger();
   if (t >= T) return;
   if (lane < k) {
     rows[warp][lane] = slot_row[(size_t)t * k + lane];
@@ -67,17 +69,16 @@ combine_kernel(const TIo* __restrict__ ye, const int32_t* __restrict__ slot_row,
 }  // namespace
 
 cudaError_t launch_combine(int dtype, const void* ye, const int32_t* slot_row, const float* w,
-                           int T, int k, int H, void* out, cudaStream_t stream) {
+                           int T, int k, int H, void* out, cudaStream_t stream, bool pdl) {
   if (T == 0) return cudaSuccess;
-  const int blocks = (T + 7) / 8;
+  const dim3 grid((T + 7) / 8), block(256);
   if (dtype == 1)
-    combine_kernel<__nv_bfloat16><<<blocks, 256, 0, stream>>>(
-        static_cast<const __nv_bfloat16*>(ye), slot_row, w, T, k, H,
-        static_cast<__nv_bfloat16*>(out));
-  else
-    combine_kernel<float><<<blocks, 256, 0, stream>>>(static_cast<const float*>(ye), slot_row, w,
-                                                      T, k, H, static_cast<float*>(out));
-  return cudaGetLastError();
+    return launch_kernel(combine_kernel<__nv_bfloat16>, grid, block, 0, stream, pdl,
+                         static_cast<const __nv_bfloat16*>(ye), slot_row, w, T, k, H,
+                         static_cast<__nv_bfloat16*>(out));
+  return launch_kernel(combine_kernel<float>, grid, block, 0, stream, pdl,
+                       static_cast<const float*>(ye), slot_row, w, T, k, H,
+                       static_cast<float*>(out));
 }
 
 }  // namespace moe

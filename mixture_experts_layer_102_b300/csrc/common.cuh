@@ -18,6 +18,36 @@ __device__ __forceinline__ void report(uint32_t* status, uint32_t bits) {
   if (status != nullptr) atomicOr(status, bits);
 }
 
+// Programmatic dependent launch. pdl_wait: block until the previous kernel of the
+// stream has completed and its writes are visible (a no-op when this kernel was not
+// launched as a dependent). pdl_trigger: let the next kernel of the stream start
+// launching. Every kernel here calls both, in that order, after a prologue that
+// touches no global memory, so at most two adjacent kernels overlap and all blocks of
+// the earlier one are already resident when the later one starts.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Launch `kernel` on `stream`, as a programmatic dependent of the previous kernel of
+// the stream when `pdl` is set.
+template <typename... Exp, typename... Act>
+inline cudaError_t launch_kernel(void (*kernel)(Exp...), dim3 grid, dim3 block, size_t smem,
+                                 cudaStream_t stream, bool pdl, Act&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, static_cast<Act&&>(args)...);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
 __device__ __forceinline__ float bf16_lo(uint32_t u) { return __uint_as_float(u << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t u) { return __uint_as_float(u & 0xFFFF0000u); }
 

@@ -22,6 +22,8 @@ gemm_simt_kernel(const float* __restrict__ A, const float* __restrict__ B0,
                  const int32_t* __restrict__ tile_expert, const int32_t* __restrict__ tile_row0,
                  const int32_t* __restrict__ offsets, const int32_t* __restrict__ num_mtiles) {
   const int mt = blockIdx.x;
+  pdl_wait();
+  pdl_trigger();
   if (mt >= *num_mtiles) return;
   const int e = tile_expert[mt];
   const int r0 = tile_row0[mt];

@@ -166,6 +166,8 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
   else __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = static_cast<uint32_t>(misc[0]);
+  pdl_wait();  // tile tables and the A rows come from earlier kernels
+  pdl_trigger();
 
   const int num_mt = *a.num_mtiles;
   const int total = num_mt * a.n_tiles;
@@ -401,7 +403,7 @@ int grid_units() {
 
 template <bool SWIGLU, int CG>
 cudaError_t launch_t(const CUtensorMap& mA, const CUtensorMap& mB0, const CUtensorMap& mB1,
-                     const TcArgs& t, cudaStream_t stream) {
+                     const TcArgs& t, cudaStream_t stream, bool pdl) {
   cudaError_t e = cudaFuncSetAttribute(grouped_gemm_tc_kernel<SWIGLU, CG>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)Shape<CG>::SMEM_BYTES);
@@ -411,13 +413,22 @@ cudaError_t launch_t(const CUtensorMap& mA, const CUtensorMap& mB0, const CUtens
   cfg.blockDim = dim3(NUM_THREADS, 1, 1);
   cfg.dynamicSmemBytes = Shape<CG>::SMEM_BYTES;
   cfg.stream = stream;
-  cudaLaunchAttribute attr;
-  attr.id = cudaLaunchAttributeClusterDimension;
-  attr.val.clusterDim.x = CG;
-  attr.val.clusterDim.y = 1;
-  attr.val.clusterDim.z = 1;
-  cfg.attrs = &attr;
-  cfg.numAttrs = CG == 2 ? 1 : 0;
+  cudaLaunchAttribute attr[2];
+  int n = 0;
+  if (CG == 2) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = CG;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  if (pdl) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
   e = cudaLaunchKernelEx(&cfg, grouped_gemm_tc_kernel<SWIGLU, CG>, mA, mB0, mB1, t);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
@@ -425,7 +436,7 @@ cudaError_t launch_t(const CUtensorMap& mA, const CUtensorMap& mB0, const CUtens
 
 }  // namespace
 
-cudaError_t launch_grouped_gemm_tc(const GroupedGemmArgs& a, cudaStream_t stream) {
+cudaError_t launch_grouped_gemm_tc(const GroupedGemmArgs& a, cudaStream_t stream, bool pdl) {
   if (a.max_mtiles == 0 || a.A_rows == 0) return cudaSuccess;
   CUtensorMap mA, mB0, mB1;
   if (!make_map(&mA, a.A, 2, (uint64_t)a.K, 0, (uint64_t)a.A_rows)) return cudaErrorInvalidValue;
@@ -447,10 +458,10 @@ cudaError_t launch_grouped_gemm_tc(const GroupedGemmArgs& a, cudaStream_t stream
   t.b1_row_off = a.swiglu ? 0 : 128;
   t.status = a.status;
   if (a.pair)
-    return a.swiglu ? launch_t<true, 2>(mA, mB0, mB1, t, stream)
-                    : launch_t<false, 2>(mA, mB0, mB1, t, stream);
-  return a.swiglu ? launch_t<true, 1>(mA, mB0, mB1, t, stream)
-                  : launch_t<false, 1>(mA, mB0, mB1, t, stream);
+    return a.swiglu ? launch_t<true, 2>(mA, mB0, mB1, t, stream, pdl)
+                    : launch_t<false, 2>(mA, mB0, mB1, t, stream, pdl);
+  return a.swiglu ? launch_t<true, 1>(mA, mB0, mB1, t, stream, pdl)
+                  : launch_t<false, 1>(mA, mB0, mB1, t, stream, pdl);
 }
 
 }  // namespace moe

@@ -1,5 +1,6 @@
 // Launchers of the MoE forward kernels, called by the C-ABI layer (moe_abi.cu).
-// Every launcher enqueues on `stream` and returns the launch status.
+// Every launcher enqueues on `stream` and returns the launch status; `pdl` launches
+// the (first) kernel as a programmatic dependent of the previous kernel of the stream.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -26,7 +27,8 @@ cudaError_t launch_router_logits(int dtype, const void* x, const void* w_router,
 int router_tc_npad(int N);
 void router_tc_split(int T, int H, int* ksplit, int* kc_per_split);
 cudaError_t launch_router_logits_tc(const void* x, const void* w_router, void* wrt, float* part,
-                                    int T, int H, int N, uint32_t* status, cudaStream_t stream);
+                                    int T, int H, int N, uint32_t* status, cudaStream_t stream,
+                                    bool pdl);
 
 // ---------------------------------------------------------------- routing decisions
 struct SelectArgs {
@@ -56,7 +58,7 @@ struct SelectArgs {
 };
 // Softmax, top-k and gate weights, capacity ranks, and (in the block that finishes
 // last) the per-expert scan, offsets, tile tables and aux loss.
-cudaError_t launch_route_select(const SelectArgs& a, int nblk, cudaStream_t stream);
+cudaError_t launch_route_select(const SelectArgs& a, int nblk, cudaStream_t stream, bool pdl);
 
 // ---------------------------------------------------------------- dispatch
 struct DispatchArgs {
@@ -75,7 +77,8 @@ struct DispatchArgs {
   int32_t* row_token;           // [A_cap]
   uint32_t* status;
 };
-cudaError_t launch_dispatch(int dtype, bool copy, const DispatchArgs& a, cudaStream_t stream);
+cudaError_t launch_dispatch(int dtype, bool copy, const DispatchArgs& a, cudaStream_t stream,
+                            bool pdl);
 
 // ---------------------------------------------------------------- experts
 struct GroupedGemmArgs {
@@ -97,10 +100,10 @@ struct GroupedGemmArgs {
 // float32 CUDA-core path (exact fp32 FMA, no TF32).
 cudaError_t launch_grouped_gemm_simt(const GroupedGemmArgs& a, cudaStream_t stream);
 // bf16 tcgen05 tensor-core path (TMA-fed, TMEM accumulators), sm_103a.
-cudaError_t launch_grouped_gemm_tc(const GroupedGemmArgs& a, cudaStream_t stream);
+cudaError_t launch_grouped_gemm_tc(const GroupedGemmArgs& a, cudaStream_t stream, bool pdl);
 
 // ---------------------------------------------------------------- combine
 cudaError_t launch_combine(int dtype, const void* ye, const int32_t* slot_row, const float* w,
-                           int T, int k, int H, void* out, cudaStream_t stream);
+                           int T, int k, int H, void* out, cudaStream_t stream, bool pdl);
 
 }  // namespace moe

@@ -32,6 +32,7 @@ struct Plan {
   int sel_tpw, n_sel_blocks;
   int max_mtiles[2];      // row tiles of 128 and of 256 rows, upper bounds
   bool pair;              // expert GEMMs on 256-row tiles (CTA pairs)
+  bool pdl;               // kernels after the first launched as programmatic dependents
   size_t elem;
   size_t off_wrt, off_part, off_psum, off_blk, off_rank, off_idx, off_w, off_drop, off_counts,
       off_kept, off_offsets, off_tile_e[2], off_tile_r[2], off_nmt, off_aux, off_slot_row,
@@ -89,6 +90,7 @@ Plan make_plan(const moe_cfg* c) {
   // CTA pairs (less shared-memory traffic per SM), small ones to single CTAs (less
   // padding of each expert's last tile, more tiles to spread over the SMs).
   p.pair = (long long)p.T * p.k >= 1024ll * p.N;
+  p.pdl = p.dtype == MOE_BF16;
 
   size_t cur = kStatusBytes;
   auto take = [&](size_t bytes) {
@@ -161,7 +163,8 @@ int run_route(const Plan& p, const void* x, const void* w_router, const float* b
   float* part = reinterpret_cast<float*>(ws + p.off_part);
   rec(0);
   if (p.dtype == MOE_BF16)
-    MOE_TRY(launch_router_logits_tc(x, w_router, ws + p.off_wrt, part, p.T, p.H, p.N, status, s));
+    MOE_TRY(launch_router_logits_tc(x, w_router, ws + p.off_wrt, part, p.T, p.H, p.N, status, s,
+                                    false));
   else
     MOE_TRY(launch_router_logits(p.dtype, x, w_router, part, p.T, p.H, p.N, p.ksplit,
                                  p.chunks_per_split, s));
@@ -190,7 +193,7 @@ int run_route(const Plan& p, const void* x, const void* w_router, const float* b
   sa.aux = o.aux;
   sa.user_counts = o.counts;
   sa.user_kept = o.kept;
-  MOE_TRY(launch_route_select(sa, p.n_sel_blocks, s));
+  MOE_TRY(launch_route_select(sa, p.n_sel_blocks, s, p.pdl));
   rec(2);
   DispatchArgs da;
   da.idx = o.idx;
@@ -207,7 +210,7 @@ int run_route(const Plan& p, const void* x, const void* w_router, const float* b
   da.slot_row = reinterpret_cast<int32_t*>(ws + p.off_slot_row);
   da.row_token = reinterpret_cast<int32_t*>(ws + p.off_row_token);
   da.status = status;
-  MOE_TRY(launch_dispatch(p.dtype, copy, da, s));
+  MOE_TRY(launch_dispatch(p.dtype, copy, da, s, p.pdl));
   rec(3);
   return MOE_OK;
 }
@@ -237,7 +240,7 @@ int run_experts(const Plan& p, const void* w1, const void* w3, const void* w2, v
   g.num_mtiles = reinterpret_cast<const int32_t*>(ws + p.off_nmt) + tb;
   g.max_mtiles = p.max_mtiles[tb];
   g.status = status;
-  if (p.dtype == MOE_BF16) MOE_TRY(launch_grouped_gemm_tc(g, s));
+  if (p.dtype == MOE_BF16) MOE_TRY(launch_grouped_gemm_tc(g, s, p.pdl));
   else MOE_TRY(launch_grouped_gemm_simt(g, s));
   rec(4);
   g.A = ws + p.off_h;
@@ -247,12 +250,12 @@ int run_experts(const Plan& p, const void* w1, const void* w3, const void* w2, v
   g.K = p.F;
   g.n_cols = p.H;
   g.swiglu = false;
-  if (p.dtype == MOE_BF16) MOE_TRY(launch_grouped_gemm_tc(g, s));
+  if (p.dtype == MOE_BF16) MOE_TRY(launch_grouped_gemm_tc(g, s, p.pdl));
   else MOE_TRY(launch_grouped_gemm_simt(g, s));
   rec(5);
   MOE_TRY(launch_combine(p.dtype, ws + p.off_ye,
                          reinterpret_cast<const int32_t*>(ws + p.off_slot_row), o.w, p.T, p.k,
-                         p.H, out, s));
+                         p.H, out, s, p.pdl));
   rec(6);
   return MOE_OK;
 }

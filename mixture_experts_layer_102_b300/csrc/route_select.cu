@@ -172,6 +172,8 @@ __global__ void __launch_bounds__(1024) route_select_kernel(SelectArgs a) {
     pw[i] = 0.f;
   }
   __syncthreads();
+  pdl_wait();  // partial logits come from the router kernel
+  pdl_trigger();
   const int NI = (N + 31) >> 5;  // experts per lane, <= 8
   const int tbase = (blockIdx.x * WARPS + warp) * a.tpw;
   // warp-local rank and expert of this lane's slot for the first MAX_TPW tokens
@@ -310,14 +312,13 @@ __global__ void __launch_bounds__(1024) route_select_kernel(SelectArgs a) {
 
 }  // namespace
 
-cudaError_t launch_route_select(const SelectArgs& a, int nblk, cudaStream_t stream) {
+cudaError_t launch_route_select(const SelectArgs& a, int nblk, cudaStream_t stream, bool pdl) {
   if (a.T == 0) return cudaSuccess;
   const size_t smem = (size_t)WARPS * a.N * 8;  // counters and P sums of every warp
   const cudaError_t e = cudaFuncSetAttribute(
       route_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  route_select_kernel<<<nblk, WARPS * 32, smem, stream>>>(a);
-  return cudaGetLastError();
+  return launch_kernel(route_select_kernel, dim3(nblk), dim3(WARPS * 32), smem, stream, pdl, a);
 }
 
 }  // namespace moe

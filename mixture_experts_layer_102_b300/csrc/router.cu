@@ -35,6 +35,8 @@ router_logits_kernel(const TIn* __restrict__ x, const TIn* __restrict__ wr,
   const int nchunk = H / KC;
   const int c_begin = blockIdx.y * chunks_per_split;
   const int c_end = min(nchunk, c_begin + chunks_per_split);
+  pdl_wait();
+  pdl_trigger();
 
   float acc[4][NJ];
 #pragma unroll

@@ -35,6 +35,8 @@ router_wt_kernel(const __nv_bfloat16* __restrict__ wr, __nv_bfloat16* __restrict
   __shared__ __nv_bfloat16 tile[32][33];
   const int h0 = blockIdx.x * 32, n0 = blockIdx.y * 32;
   const int tx = threadIdx.x, ty = threadIdx.y;
+  pdl_wait();
+  pdl_trigger();
   for (int j = ty; j < 32; j += 8) {
     const int h = h0 + j, n = n0 + tx;
     tile[j][tx] = (h < H && n < N) ? wr[(size_t)h * N + n] : __float2bfloat16(0.f);
@@ -97,6 +99,8 @@ router_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = static_cast<uint32_t>(misc[0]);
+  pdl_wait();  // W_rT comes from the previous kernel
+  pdl_trigger();
 
   if (warp == 0) {
     if (lane == 0) {  // ---------------------------------------------- TMA producer
@@ -207,13 +211,14 @@ void router_tc_split(int T, int H, int* ksplit, int* kc_per_split) {
 }
 
 cudaError_t launch_router_logits_tc(const void* x, const void* w_router, void* wrt, float* part,
-                                    int T, int H, int N, uint32_t* status, cudaStream_t stream) {
+                                    int T, int H, int N, uint32_t* status, cudaStream_t stream,
+                                    bool pdl) {
   if (T == 0) return cudaSuccess;
   const int n_pad = router_tc_npad(N);
-  router_wt_kernel<<<dim3((H + 31) / 32, (n_pad + 31) / 32), dim3(32, 8), 0, stream>>>(
-      static_cast<const __nv_bfloat16*>(w_router), static_cast<__nv_bfloat16*>(wrt), H, N,
-      n_pad);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_kernel(router_wt_kernel, dim3((H + 31) / 32, (n_pad + 31) / 32),
+                                dim3(32, 8), 0, stream, pdl,
+                                static_cast<const __nv_bfloat16*>(w_router),
+                                static_cast<__nv_bfloat16*>(wrt), H, N, n_pad);
   if (e != cudaSuccess) return e;
   CUtensorMap mX, mW;
   if (!make_map(&mX, x, 2, (uint64_t)H, 0, (uint64_t)T, 128)) return cudaErrorInvalidValue;
@@ -240,8 +245,8 @@ cudaError_t launch_router_logits_tc(const void* x, const void* w_router, void* w
   e = cudaFuncSetAttribute(router_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)smem);
   if (e != cudaSuccess) return e;
-  router_tc_kernel<<<dim3((T + 127) / 128, ksplit), NUM_THREADS, smem, stream>>>(mX, mW, a);
-  return cudaGetLastError();
+  return launch_kernel(router_tc_kernel, dim3((T + 127) / 128, ksplit), dim3(NUM_THREADS), smem,
+                       stream, true, mX, mW, a);
 }
 
 }  // namespace moe
