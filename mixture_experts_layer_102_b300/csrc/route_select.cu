@@ -47,22 +47,24 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-// Column scan of the per-block counts by the last block (1024 threads): G threads
-// share an expert column and each walks a contiguous range of block rows.
+// The last block's scan (1024 threads). Thread (g, col) walks a contiguous range of
+// block rows of one expert column; a warp covers consecutive columns of the same rows,
+// so its loads are coalesced. A parallel prefix over the row groups gives every group
+// its base, and warp 0 scans the experts for offsets and tile starts.
 __device__ void finish_routing(const SelectArgs& a, int nblk) {
-  __shared__ int32_t ipart[1024];
-  __shared__ float fpart[1024];
+  __shared__ int32_t ip[1024];
+  __shared__ float fq[1024];
   __shared__ int32_t s_counts[256], s_kept[256], s_off[257], s_tile0[2][257];
   __shared__ float s_psum[256];
   const int tid = threadIdx.x;
   const int N = a.N;
   int np2 = 1;
   while (np2 < N) np2 <<= 1;
-  const int G = 1024 / np2;
-  const int col = tid / G, g = tid - col * G;
+  const int G = 1024 / np2;                 // row groups
+  const int col = tid % np2, g = tid / np2;
   const int R = (nblk + G - 1) / G;
   const int r0 = min(nblk, g * R), r1 = min(nblk, r0 + R);
-  constexpr int B = 8;  // rows per batch: B loads in flight per thread
+  constexpr int B = 8;                      // rows per batch: B loads in flight per thread
   int isum = 0;
   float fsum = 0.f;
   if (col < N) {
@@ -82,30 +84,31 @@ __device__ void finish_routing(const SelectArgs& a, int nblk) {
       }
     }
   }
-  ipart[tid] = isum;
-  fpart[tid] = fsum;
+  ip[tid] = isum;
+  fq[tid] = fsum;
   __syncthreads();
-  if (col < N && g == 0) {
-    int run = 0;
-    float p = 0.f;
-    for (int q = 0; q < G; ++q) {
-      const int v = ipart[tid + q];
-      ipart[tid + q] = run;
-      run += v;
-      p += fpart[tid + q];
-    }
+  // inclusive prefix over the row groups of each column (fixed pattern: deterministic)
+  for (int d = 1; d < G; d <<= 1) {
+    const int iv = g >= d ? ip[tid - d * np2] : 0;
+    const float fv = g >= d ? fq[tid - d * np2] : 0.f;
+    __syncthreads();
+    ip[tid] += iv;
+    fq[tid] += fv;
+    __syncthreads();
+  }
+  if (col < N && g == G - 1) {
+    const int run = ip[tid];
     const int kept = (a.C < 0 || (long long)run <= a.C) ? run : (int)a.C;
     s_counts[col] = run;
     s_kept[col] = kept;
-    s_psum[col] = p;
+    s_psum[col] = fq[tid];
     a.counts[col] = run;
     a.kept[col] = kept;
     if (a.user_counts != nullptr) a.user_counts[col] = run;
     if (a.user_kept != nullptr) a.user_kept[col] = kept;
   }
-  __syncthreads();
   if (col < N) {  // exclusive per-expert base of every block
-    int run = ipart[tid];
+    int run = ip[tid] - isum;
     for (int rb = r0; rb < r1; rb += B) {
       int iv[B];
 #pragma unroll
@@ -118,29 +121,55 @@ __device__ void finish_routing(const SelectArgs& a, int nblk) {
       }
     }
   }
-  if (tid == 0) {
-    int off = 0, tiles1 = 0, tiles2 = 0;
+  __syncthreads();
+  if (tid < 32) {  // warp 0: offsets, tile starts and the aux loss over the experts
+    const int lane = tid;
+    const int per = (N + 31) / 32;  // experts per lane, <= 8
+    const int e0 = min(N, lane * per), e1 = min(N, e0 + per);
+    int off = 0, t1 = 0, t2 = 0;
     float fp = 0.f;
-    for (int e = 0; e < N; ++e) {
-      s_off[e] = off;
-      s_tile0[0][e] = tiles1;
-      s_tile0[1][e] = tiles2;
-      a.offsets[e] = off;
+    for (int e = e0; e < e1; ++e) {
       off += s_kept[e];
-      tiles1 += (s_kept[e] + TILE_ROWS_1 - 1) / TILE_ROWS_1;
-      tiles2 += (s_kept[e] + TILE_ROWS_2 - 1) / TILE_ROWS_2;
+      t1 += (s_kept[e] + TILE_ROWS_1 - 1) / TILE_ROWS_1;
+      t2 += (s_kept[e] + TILE_ROWS_2 - 1) / TILE_ROWS_2;
       fp = fmaf((float)s_counts[e], s_psum[e], fp);
     }
-    s_off[N] = off;
-    s_tile0[0][N] = tiles1;
-    s_tile0[1][N] = tiles2;
-    a.offsets[N] = off;
-    *a.num_mtiles[0] = tiles1;
-    *a.num_mtiles[1] = tiles2;
-    // aux = N * sum_e (counts_e / (T*k)) * (Psum_e / T); counts <= T*k and
-    // sum_e Psum_e = T keep every term well inside fp32 range
-    const float Tf = (float)a.T;
-    *a.aux = a.T > 0 ? (float)N * (fp / (Tf * (float)a.k)) / Tf : 0.f;
+    int xo = off, x1 = t1, x2 = t2;  // inclusive scans over the lanes
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int po = __shfl_up_sync(0xffffffffu, xo, d);
+      const int p1 = __shfl_up_sync(0xffffffffu, x1, d);
+      const int p2 = __shfl_up_sync(0xffffffffu, x2, d);
+      if (lane >= d) {
+        xo += po;
+        x1 += p1;
+        x2 += p2;
+      }
+    }
+    int o = xo - off, a1 = x1 - t1, a2 = x2 - t2;
+    for (int e = e0; e < e1; ++e) {
+      s_off[e] = o;
+      s_tile0[0][e] = a1;
+      s_tile0[1][e] = a2;
+      a.offsets[e] = o;
+      o += s_kept[e];
+      a1 += (s_kept[e] + TILE_ROWS_1 - 1) / TILE_ROWS_1;
+      a2 += (s_kept[e] + TILE_ROWS_2 - 1) / TILE_ROWS_2;
+    }
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) fp += __shfl_xor_sync(0xffffffffu, fp, d);
+    if (lane == 31) {
+      s_off[N] = xo;
+      s_tile0[0][N] = x1;
+      s_tile0[1][N] = x2;
+      a.offsets[N] = xo;
+      *a.num_mtiles[0] = x1;
+      *a.num_mtiles[1] = x2;
+      // aux = N * sum_e (counts_e / (T*k)) * (Psum_e / T); counts <= T*k and
+      // sum_e Psum_e = T keep every term well inside fp32 range
+      const float Tf = (float)a.T;
+      *a.aux = a.T > 0 ? (float)N * (fp / (Tf * (float)a.k)) / Tf : 0.f;
+    }
   }
   __syncthreads();
 #pragma unroll
@@ -187,6 +216,7 @@ __global__ void __launch_bounds__(1024) route_select_kernel(SelectArgs a) {
 #pragma unroll
     for (int q = 0; q < 8; ++q) v[q] = (q < NI && lane + 32 * q < N) ? 0.f : -INFINITY;
     // sum the split partials in split order; the loads of one split are independent
+#pragma unroll 4
     for (int p = 0; p < a.ksplit; ++p) {
       const float* row = a.part + ((size_t)p * a.T + t) * N;
 #pragma unroll
