@@ -342,37 +342,79 @@ def run_gpu_arm(args, cfg):
         for s in range(len(STAGES)):
             stage_ms[i, s] = evs[s].elapsed_time(evs[s + 1])
 
-    # end to end through the public API: pinned host x in, host out back, every step
+    # End to end through the public API: every step copies its x from pinned host
+    # memory to the device and its out and aux back to pinned host memory. Pipelined
+    # as a serving loop would run it: the copy-in of step i+1 and the copy-out of step
+    # i run on their own streams beside the forward of step i (double buffers ordered
+    # by events). The fully serial loop (copy, forward, copy, synchronise) is also
+    # reported.
     e2e = None
     if not args.no_e2e:
-        x_host = moe.to_torch(inp.x, cfg.dtype).pin_memory()
-        out_host = torch.empty((cfg.T, cfg.H), dtype=dev.x.dtype).pin_memory()
-        aux_host = torch.empty(1, dtype=torch.float32).pin_memory()
-        x_dev = torch.empty_like(dev.x)
-
-        def e2e_step():
-            x_dev.copy_(x_host, non_blocking=True)
-            moe.forward(c, x_dev, dev.w_router, dev.router_bias, dev.w1, dev.w3, dev.w2,
-                        workspace=ws, out=out, routing=routing, stream=stream)
-            out_host.copy_(out, non_blocking=True)
-            aux_host.copy_(routing.aux_loss, non_blocking=True)
-            stream.synchronize()
-
-        for _ in range(max(3, args.warmup)):
-            e2e_step()
         n_e2e = min(args.steps, 200)
+        b = 2 if cfg.dtype == "bf16" else 4
+        x_host = [moe.to_torch(inputs.make_x(cfg, rank=rank * 7919 + 1 + j), cfg.dtype).pin_memory()
+                  for j in range(2)]
+        out_host = [torch.empty((cfg.T, cfg.H), dtype=dev.x.dtype).pin_memory() for _ in range(2)]
+        aux_host = [torch.empty(1, dtype=torch.float32).pin_memory() for _ in range(2)]
+        x_dev = [torch.empty_like(dev.x) for _ in range(2)]
+        out_dev = [torch.empty_like(out) for _ in range(2)]
+        rts = [moe.new_routing(c, device) for _ in range(2)]
+        s_in = torch.cuda.Stream(device)
+        s_out = torch.cuda.Stream(device)
+        ev_in = [torch.cuda.Event() for _ in range(2)]
+        ev_fwd = [torch.cuda.Event() for _ in range(2)]
+        ev_out = [torch.cuda.Event() for _ in range(2)]
+
+        def run_pipelined(n):
+            for i in range(n):
+                j = i % 2
+                with torch.cuda.stream(s_in):
+                    if i >= 2:
+                        s_in.wait_event(ev_fwd[j])        # step i-2 no longer reads x_dev[j]
+                    x_dev[j].copy_(x_host[j], non_blocking=True)
+                    ev_in[j].record(s_in)
+                stream.wait_event(ev_in[j])
+                if i >= 2:
+                    stream.wait_event(ev_out[j])          # step i-2's out has been copied out
+                moe.forward(c, x_dev[j], dev.w_router, dev.router_bias, dev.w1, dev.w3, dev.w2,
+                            workspace=ws, out=out_dev[j], routing=rts[j], stream=stream)
+                ev_fwd[j].record(stream)
+                with torch.cuda.stream(s_out):
+                    s_out.wait_event(ev_fwd[j])
+                    out_host[j].copy_(out_dev[j], non_blocking=True)
+                    aux_host[j].copy_(rts[j].aux_loss, non_blocking=True)
+                    ev_out[j].record(s_out)
+            torch.cuda.synchronize(device)
+
+        def run_serial(n):
+            for i in range(n):
+                j = i % 2
+                x_dev[j].copy_(x_host[j], non_blocking=True)
+                moe.forward(c, x_dev[j], dev.w_router, dev.router_bias, dev.w1, dev.w3, dev.w2,
+                            workspace=ws, out=out_dev[j], routing=rts[j], stream=stream)
+                out_host[j].copy_(out_dev[j], non_blocking=True)
+                aux_host[j].copy_(rts[j].aux_loss, non_blocking=True)
+                stream.synchronize()
+
+        run_pipelined(max(3, args.warmup))
         barrier(world, device)
         t0 = time.perf_counter()
-        for _ in range(n_e2e):
-            e2e_step()
-        e2e_s = (time.perf_counter() - t0) / n_e2e
-        e2e_s = reduce_max(e2e_s, world, device)
+        run_pipelined(n_e2e)
+        pipe_s = reduce_max((time.perf_counter() - t0) / n_e2e, world, device)
+        run_serial(3)
+        barrier(world, device)
+        t0 = time.perf_counter()
+        run_serial(n_e2e)
+        serial_s = reduce_max((time.perf_counter() - t0) / n_e2e, world, device)
         moe.get_status(ws)
-        b = 2 if cfg.dtype == "bf16" else 4
-        e2e = {"value": total_tokens / e2e_s, "unit": UNIT,
+        e2e = {"value": round(total_tokens / pipe_s, 1), "unit": UNIT,
                "h2d_bytes_per_step": cfg.T * cfg.H * b,
                "d2h_bytes_per_step": cfg.T * cfg.H * b + 4,
-               "ms_per_step": e2e_s * 1e3, "steps": n_e2e}
+               "ms_per_step": round(pipe_s * 1e3, 5), "steps": n_e2e,
+               "mode": "pipelined: copy-in of step i+1 and copy-out of step i on their "
+                       "own streams beside the forward of step i",
+               "serial_value": round(total_tokens / serial_s, 1),
+               "serial_ms_per_step": round(serial_s * 1e3, 5)}
 
     if rank != 0:
         return None

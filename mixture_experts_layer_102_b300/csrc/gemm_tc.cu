@@ -78,16 +78,28 @@ __host__ __device__ constexpr uint32_t idesc() {
 // negative z and the quotient then reads 0, the limit of silu.
 __device__ __forceinline__ float silu_fast(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
 
-// Work item w -> (row tile, column tile): bands of GROUP_M row tiles, row tile
-// fastest inside a band, so the pairs in flight share a few A and B tiles in L2.
-__device__ __forceinline__ void raster(int w, int num_mt, int n_tiles, int& mt, int& nt) {
+// Work item w -> (row tile, column tile). Items are grouped by expert (an expert's
+// tiles x all column tiles, experts in order); inside an expert, bands of GROUP_M row
+// tiles sweep the column tiles with the row tile fastest, so the units in flight share
+// a few A tiles and each weight tile of the expert is streamed about once per band.
+// `tfirst` [N+1] holds each expert's first row tile (shared memory).
+__device__ __forceinline__ void raster(int w, const int32_t* tfirst, int N, int n_tiles, int& mt,
+                                       int& nt) {
+  int lo = 0, hi = N - 1;  // last expert whose first item is <= w
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (tfirst[mid] * n_tiles <= w) lo = mid; else hi = mid - 1;
+  }
+  const int t0 = tfirst[lo];
+  const int tiles = tfirst[lo + 1] - t0;
+  const int local = w - t0 * n_tiles;
   const int band_size = GROUP_M * n_tiles;
-  const int band = w / band_size;
-  const int local = w - band * band_size;
+  const int band = local / band_size;
+  const int in_band = local - band * band_size;
   const int m_first = band * GROUP_M;
-  const int gm = min(GROUP_M, num_mt - m_first);
-  mt = m_first + local % gm;
-  nt = local / gm;
+  const int gm = min(GROUP_M, tiles - m_first);
+  mt = t0 + m_first + in_band % gm;
+  nt = in_band / gm;
 }
 
 struct TcArgs {
@@ -95,6 +107,8 @@ struct TcArgs {
   const int32_t* tile_row0;
   const int32_t* offsets;
   const int32_t* num_mtiles;
+  const int32_t* tile_first;  // [N+1] first row tile of each expert
+  int N;
   __nv_bfloat16* out;
   int out_ld;        // output row stride (elements)
   int K;             // reduction length, multiple of 64
@@ -169,6 +183,9 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
   pdl_wait();  // tile tables and the A rows come from earlier kernels
   pdl_trigger();
 
+  __shared__ int32_t tfirst[257];
+  for (int i = threadIdx.x; i <= a.N; i += blockDim.x) tfirst[i] = a.tile_first[i];
+  __syncthreads();
   const int num_mt = *a.num_mtiles;
   const int total = num_mt * a.n_tiles;
   const int kchunks = a.K / BK;
@@ -185,7 +202,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
       bool ok = true;
       for (int w = unit; w < total && ok; w += num_units) {
         int mt, nt;
-        raster(w, num_mt, a.n_tiles, mt, nt);
+        raster(w, tfirst, a.N, a.n_tiles, mt, nt);
         const int e = a.tile_expert[mt];
         const int row0 = a.tile_row0[mt] + (int)rank * 128;
         const int n0 = nt * a.n_per_tile;
@@ -282,7 +299,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
     uint32_t acc_phase = 0;
     for (int w = unit; w < total; w += num_units) {
       int mt, nt;
-      raster(w, num_mt, a.n_tiles, mt, nt);
+      raster(w, tfirst, a.N, a.n_tiles, mt, nt);
       const int e = a.tile_expert[mt];
       const int r = a.tile_row0[mt] + (int)rank * 128 + row_in_cta;
       const bool valid = r < a.offsets[e + 1];
@@ -449,6 +466,8 @@ cudaError_t launch_grouped_gemm_tc(const GroupedGemmArgs& a, cudaStream_t stream
   t.tile_row0 = a.tile_row0;
   t.offsets = a.offsets;
   t.num_mtiles = a.num_mtiles;
+  t.tile_first = a.tile_first;
+  t.N = a.N;
   t.out = static_cast<__nv_bfloat16*>(a.out);
   t.out_ld = a.n_cols;
   t.K = a.K;

@@ -52,6 +52,7 @@ struct SelectArgs {
   int32_t* tile_expert[2];
   int32_t* tile_row0[2];
   int32_t* num_mtiles[2];
+  int32_t* tile_first[2];       // [N+1] first tile of each expert (and the total)
   float* aux;                   // [1]
   int32_t* user_counts;         // optional copies for the caller
   int32_t* user_kept;
@@ -94,6 +95,7 @@ struct GroupedGemmArgs {
   const int32_t* tile_row0;
   const int32_t* offsets;
   const int32_t* num_mtiles;
+  const int32_t* tile_first;    // [N+1] first tile of each expert in that table
   int max_mtiles;
   uint32_t* status;
 };

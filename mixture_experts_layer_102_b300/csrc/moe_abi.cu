@@ -35,7 +35,8 @@ struct Plan {
   bool pdl;               // kernels after the first launched as programmatic dependents
   size_t elem;
   size_t off_wrt, off_part, off_psum, off_blk, off_rank, off_idx, off_w, off_drop, off_counts,
-      off_kept, off_offsets, off_tile_e[2], off_tile_r[2], off_nmt, off_aux, off_slot_row,
+      off_kept, off_offsets, off_tile_e[2], off_tile_r[2], off_tile_f[2], off_nmt, off_aux,
+      off_slot_row,
       off_row_token, off_xp, off_h, off_ye, total;
 };
 
@@ -113,6 +114,7 @@ Plan make_plan(const moe_cfg* c) {
   for (int tb = 0; tb < 2; ++tb) {
     p.off_tile_e[tb] = take((size_t)p.max_mtiles[tb] * 4);
     p.off_tile_r[tb] = take((size_t)p.max_mtiles[tb] * 4);
+    p.off_tile_f[tb] = take((N + 1) * 4);
   }
   p.off_nmt = take(8);
   p.off_aux = take(4);
@@ -189,6 +191,7 @@ int run_route(const Plan& p, const void* x, const void* w_router, const float* b
     sa.tile_expert[tb] = reinterpret_cast<int32_t*>(ws + p.off_tile_e[tb]);
     sa.tile_row0[tb] = reinterpret_cast<int32_t*>(ws + p.off_tile_r[tb]);
     sa.num_mtiles[tb] = reinterpret_cast<int32_t*>(ws + p.off_nmt) + tb;
+    sa.tile_first[tb] = reinterpret_cast<int32_t*>(ws + p.off_tile_f[tb]);
   }
   sa.aux = o.aux;
   sa.user_counts = o.counts;
@@ -238,6 +241,7 @@ int run_experts(const Plan& p, const void* w1, const void* w3, const void* w2, v
   g.tile_row0 = reinterpret_cast<const int32_t*>(ws + p.off_tile_r[tb]);
   g.offsets = reinterpret_cast<const int32_t*>(ws + p.off_offsets);
   g.num_mtiles = reinterpret_cast<const int32_t*>(ws + p.off_nmt) + tb;
+  g.tile_first = reinterpret_cast<const int32_t*>(ws + p.off_tile_f[tb]);
   g.max_mtiles = p.max_mtiles[tb];
   g.status = status;
   if (p.dtype == MOE_BF16) MOE_TRY(launch_grouped_gemm_tc(g, s, p.pdl));

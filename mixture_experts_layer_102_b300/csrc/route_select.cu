@@ -151,6 +151,8 @@ __device__ void finish_routing(const SelectArgs& a, int nblk) {
       s_off[e] = o;
       s_tile0[0][e] = a1;
       s_tile0[1][e] = a2;
+      a.tile_first[0][e] = a1;
+      a.tile_first[1][e] = a2;
       a.offsets[e] = o;
       o += s_kept[e];
       a1 += (s_kept[e] + TILE_ROWS_1 - 1) / TILE_ROWS_1;
@@ -163,6 +165,8 @@ __device__ void finish_routing(const SelectArgs& a, int nblk) {
       s_tile0[0][N] = x1;
       s_tile0[1][N] = x2;
       a.offsets[N] = xo;
+      a.tile_first[0][N] = x1;
+      a.tile_first[1][N] = x2;
       *a.num_mtiles[0] = x1;
       *a.num_mtiles[1] = x2;
       // aux = N * sum_e (counts_e / (T*k)) * (Psum_e / T); counts <= T*k and
