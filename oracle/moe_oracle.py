@@ -34,6 +34,23 @@ Readings where the pages are open (each also listed in the design notes):
   (no renormalisation); the layer returns only the MoE branch, the caller adds the
   residual, so a token with every slot dropped gets exactly 0.
 * T = 0 gives aux = 0 (empty sums).
+
+Options beyond the base layer (the pages' further variants):
+* shared experts (hotelren.com/news/5904824 section 3.3): ``n_shared`` always-on experts
+  whose weights follow the routed ones; every valid token adds their outputs with
+  weight 1; they take no capacity and stay out of the router and the aux losses.
+* the two-layer GELU expert W2 gelu(W1 x) (devpress.csdn.net MoE page section 4.1),
+  exact (erf) GELU.
+* a valid-token mask (devpress.csdn.net MoE page section 5.2: capacity counts only
+  non-padding tokens). Reading: padding tokens are routed as if they were not in the
+  batch at all -- everything (counts, capacity with T_valid, ranks, aux losses) is the
+  layer on the valid tokens alone; padding tokens get no expert (index -1, weight 0,
+  dropped) and output 0.
+* two more balance losses: KL(uniform || f) with f_e = counts_e / (T*k)
+  (hotelren.com/news/3071227 section 4.2 takes the KL divergence of the expert load
+  to the uniform target; its load is normalised by the mask size, here by T*k so that
+  f is a distribution), and the unbiased variance of all router probabilities
+  (2kiu.com/news/2885792 section 5.1: lambda * std(router_probs)**2, without lambda).
 """
 from __future__ import annotations
 
@@ -113,6 +130,27 @@ def aux_loss(probs: np.ndarray, idx: np.ndarray, N: int, k: int) -> float:
     return float(N * np.sum(f * P))
 
 
+def aux_kl_uniform(idx: np.ndarray, N: int, k: int) -> float:
+    """KL(uniform || f) = sum_e (1/N) log((1/N) / f_e), f_e = counts_e/(T*k); +inf
+    when an expert receives no slot, 0 for an empty batch."""
+    T = idx.shape[0]
+    if T == 0:
+        return 0.0
+    f = expert_counts(idx, N) / float(T * k)
+    with np.errstate(divide="ignore"):
+        return float(np.sum((1.0 / N) * (np.log(1.0 / N) - np.log(f))))
+
+
+def aux_prob_variance(probs: np.ndarray) -> float:
+    """Unbiased variance over all entries of the router probabilities (torch.std's
+    default correction), squared std; 0 for an empty batch."""
+    if probs.size == 0:
+        return 0.0
+    if probs.size == 1:
+        return float("nan")
+    return float(np.var(probs, ddof=1))
+
+
 def capacity_assign(idx: np.ndarray, N: int, C: Optional[int]):
     """Walk the slots in token order (t ascending, then slot s) and give each the
     number of earlier slots that chose the same expert. A slot is dropped when that
@@ -147,6 +185,24 @@ def swiglu_expert(x_rows: np.ndarray, w1_e: np.ndarray, w3_e: np.ndarray,
     g = xr @ np.asarray(w1_e, np.float64).T
     u = xr @ np.asarray(w3_e, np.float64).T
     return (silu(g) * u) @ np.asarray(w2_e, np.float64).T
+
+
+def gelu(z: np.ndarray) -> np.ndarray:
+    """Exact GELU: z * Phi(z) = 0.5 z (1 + erf(z / sqrt(2)))."""
+    from scipy.special import erf
+    return 0.5 * z * (1.0 + erf(z / math.sqrt(2.0)))
+
+
+def gelu_expert(x_rows: np.ndarray, w1_e: np.ndarray, w2_e: np.ndarray) -> np.ndarray:
+    """The two-layer expert: W2 gelu(W1 x)."""
+    xr = np.asarray(x_rows, np.float64)
+    return gelu(xr @ np.asarray(w1_e, np.float64).T) @ np.asarray(w2_e, np.float64).T
+
+
+def expert_ffn(x_rows, w1_e, w3_e, w2_e, activation: str = "swiglu") -> np.ndarray:
+    if activation == "gelu":
+        return gelu_expert(x_rows, w1_e, w2_e)
+    return swiglu_expert(x_rows, w1_e, w3_e, w2_e)
 
 
 def near_tie_tokens(logits: np.ndarray, k: int, margin: float = NEAR_TIE_MARGIN):
@@ -189,10 +245,16 @@ class OracleResult:
     out: np.ndarray             # [len(tokens), H] float64
     near_tie_set: np.ndarray
     near_tie_order: np.ndarray
+    aux_kl: float = 0.0
+    aux_std2: float = 0.0
 
 
-def route(x, w_router, bias, k: int, capacity_factor):
-    """Steps 1-5 for every token."""
+def route(x, w_router, bias, k: int, capacity_factor, valid_mask=None):
+    """Steps 1-5 for every token. With ``valid_mask``, the valid tokens are routed as
+    a batch of their own and the padding tokens get index -1, weight 0, dropped."""
+    if valid_mask is not None:
+        return _route_masked(x, w_router, bias, k, capacity_factor,
+                             np.asarray(valid_mask).astype(bool))
     T = x.shape[0]
     N = w_router.shape[1]
     logits = router_logits(x, w_router, bias)
@@ -205,18 +267,42 @@ def route(x, w_router, bias, k: int, capacity_factor):
     rank, drop, kept = capacity_assign(idx, N, C)
     set_ties, order_ties = near_tie_tokens(logits, k)
     return dict(logits=logits, probs=probs, topk_idx=idx, topk_w=w, aux_loss=aux,
+                aux_kl=aux_kl_uniform(idx, N, k), aux_std2=aux_prob_variance(probs),
                 expert_counts=counts, capacity=C, rank=rank, drop_mask=drop,
                 kept_counts=kept, near_tie_set=set_ties, near_tie_order=order_ties)
 
 
+def _route_masked(x, w_router, bias, k, capacity_factor, valid):
+    T = x.shape[0]
+    v = np.nonzero(valid)[0]
+    r = route(np.asarray(x)[v], w_router, bias, k, capacity_factor)
+    full = dict(r)
+    full["logits"] = router_logits(x, w_router, bias)
+    full["probs"] = full_softmax(full["logits"])
+    idx = np.full((T, k), -1, dtype=np.int64)
+    idx[v] = r["topk_idx"]
+    w = np.zeros((T, k))
+    w[v] = r["topk_w"]
+    rank = np.full((T, k), -1, dtype=np.int64)
+    rank[v] = r["rank"]
+    drop = np.ones((T, k), dtype=np.uint8)
+    drop[v] = r["drop_mask"]
+    full.update(topk_idx=idx, topk_w=w, rank=rank, drop_mask=drop,
+                near_tie_set=v[r["near_tie_set"]], near_tie_order=v[r["near_tie_order"]],
+                valid_tokens=v)
+    return full
+
+
 def moe_forward(x, w_router, bias, w1, w3, w2, k: int, capacity_factor,
-                token_sample: Optional[np.ndarray] = None) -> OracleResult:
+                token_sample: Optional[np.ndarray] = None, n_shared: int = 0,
+                activation: str = "swiglu", valid_mask=None) -> OracleResult:
     """The whole layer. Routing and capacity always cover every token (capacity
     depends on token order); the expert FFN and the combine are evaluated for the
-    tokens in ``token_sample`` (all tokens when None)."""
+    tokens in ``token_sample`` (all tokens when None). w1/w3/w2 hold the N routed
+    experts followed by ``n_shared`` shared ones (w3 unused for GELU experts)."""
     T, H = x.shape
     N = w_router.shape[1]
-    r = route(x, w_router, bias, k, capacity_factor)
+    r = route(x, w_router, bias, k, capacity_factor, valid_mask)
     tokens = np.arange(T) if token_sample is None else np.asarray(token_sample, np.int64)
     out = np.zeros((len(tokens), H), dtype=np.float64)
     idx, w, drop = r["topk_idx"], r["topk_w"], r["drop_mask"]
@@ -234,6 +320,18 @@ def moe_forward(x, w_router, bias, w1, w3, w2, k: int, capacity_factor,
         rows = np.asarray(rows)
         slots = np.asarray(slots)
         # A token visits an expert at most once, so ``rows`` has no repeats here.
-        ye = swiglu_expert(np.asarray(x[tokens[rows]], np.float64), w1[e], w3[e], w2[e])
+        ye = expert_ffn(np.asarray(x[tokens[rows]], np.float64), w1[e],
+                        None if w3 is None else w3[e], w2[e], activation)
         out[rows] += w[tokens[rows], slots][:, None] * ye
+    if n_shared:
+        live = np.arange(len(tokens))
+        if valid_mask is not None:
+            live = live[np.asarray(valid_mask).astype(bool)[tokens]]
+        if len(live):
+            xs = np.asarray(x[tokens[live]], np.float64)
+            for j in range(n_shared):
+                e = N + j
+                out[live] += expert_ffn(xs, w1[e], None if w3 is None else w3[e], w2[e],
+                                        activation)
+    r = {key: val for key, val in r.items() if key in OracleResult.__dataclass_fields__}
     return OracleResult(out=out, tokens=tokens, **r)

@@ -50,8 +50,8 @@ def test_aux_without_division_by_k_is_caught(monkeypatch):
 def test_aux_after_capacity_is_caught(monkeypatch):
     real_route = om.route
 
-    def route_post_cap(x, w_router, bias, k, cf):
-        r = real_route(x, w_router, bias, k, cf)
+    def route_post_cap(x, w_router, bias, k, cf, valid_mask=None):
+        r = real_route(x, w_router, bias, k, cf, valid_mask)
         T, N = r["logits"].shape
         if T:
             f = r["kept_counts"] / float(T * k)
@@ -102,8 +102,8 @@ def test_capacity_priority_reversed_is_caught(monkeypatch):
 def test_renormalising_after_a_drop_is_caught(monkeypatch):
     real_route = om.route
 
-    def route_renorm(x, w_router, bias, k, cf):
-        r = real_route(x, w_router, bias, k, cf)
+    def route_renorm(x, w_router, bias, k, cf, valid_mask=None):
+        r = real_route(x, w_router, bias, k, cf, valid_mask)
         w = r["topk_w"] * (1 - r["drop_mask"])
         s = w.sum(axis=1, keepdims=True)
         r["topk_w"] = np.where(s > 0, w / np.where(s > 0, s, 1.0), 0.0)
@@ -115,8 +115,8 @@ def test_renormalising_after_a_drop_is_caught(monkeypatch):
 def test_ignoring_drops_in_the_combine_is_caught(monkeypatch):
     real_route = om.route
 
-    def route_no_drop(x, w_router, bias, k, cf):
-        r = real_route(x, w_router, bias, k, cf)
+    def route_no_drop(x, w_router, bias, k, cf, valid_mask=None):
+        r = real_route(x, w_router, bias, k, cf, valid_mask)
         r["drop_mask"] = np.zeros_like(r["drop_mask"])
         return r
     _plant(monkeypatch, "route", route_no_drop)
