@@ -185,6 +185,74 @@ int moe_route_static(const moe_cfg* cfg, const void* x, const void* w_router,
                      float* aux_loss, uint8_t* drop_mask, int32_t* expert_counts,
                      int32_t* kept_counts, void* stream);
 
+/*
+ * ---------------------------------------------------------------------------
+ * Layer options: the variants the pages describe beyond the base layer. The
+ * *_ex calls take a moe_options pointer; NULL means the base layer, exactly as
+ * moe_workspace_size / moe_route / moe_forward_timed compute it.
+ * ---------------------------------------------------------------------------
+ */
+
+/* Expert FFN. SWIGLU: W2 (silu(W1 x) * (W3 x)) (2kiu.com/news/2885792 section 2.2).
+ * GELU: the two-layer expert W2 gelu(W1 x) with the exact (erf) GELU
+ * (devpress.csdn.net MoE page section 4.1); w3 is not read and may be NULL. */
+typedef enum { MOE_ACT_SWIGLU = 0, MOE_ACT_GELU = 1 } moe_activation;
+
+/* Most shared experts one layer may have. */
+#define MOE_MAX_SHARED 8
+
+typedef struct {
+  /* Shared experts (hotelren.com/news/5904824 section 3.3): always-on experts that
+   * every valid token runs with weight 1, beside its k routed ones. They take no
+   * capacity and stay out of the router, the counts and the losses. Their weights
+   * follow the routed experts' in w1, w3, w2, which then hold N + n_shared experts
+   * ([N+n_shared, F, H] and [N+n_shared, H, F]). 0 <= n_shared <= MOE_MAX_SHARED. */
+  int32_t n_shared;
+  /* moe_activation of every expert, routed and shared. */
+  int32_t activation;
+  /* [T] device bytes, 1 = real token, 0 = padding; NULL = every token is real.
+   * Capacity counts only the real tokens (devpress.csdn.net MoE page section 5.2):
+   * the layer treats the real tokens as its whole batch (T_valid of them, in token
+   * order) for the counts, C = ceil(CF*T_valid*k/N), the ranks and every loss. A
+   * padding token gets topk_idx -1, topk_w 0, every slot dropped, and out = 0. */
+  const uint8_t* valid_mask;
+  /* [1] device float32 or NULL: KL(uniform || f) with f_e = counts_e/(T_valid*k)
+   * (hotelren.com/news/3071227 section 4.2 takes the KL divergence of the expert
+   * load to the uniform target); +inf when some expert receives no slot; 0 when
+   * T_valid = 0. */
+  float* aux_kl;
+  /* [1] device float32 or NULL: the unbiased variance (the square of the sample
+   * standard deviation) of all T_valid*N router probabilities
+   * (2kiu.com/news/2885792 section 5.1 penalises std(router_probs)^2); 0 when
+   * T_valid = 0, NaN when T_valid*N = 1. */
+  float* aux_std2;
+} moe_options;
+
+/* Workspace bytes for cfg with opts (NULL opts: moe_workspace_size); 0 when cfg
+ * or opts is invalid or unsupported. Pure host function. */
+size_t moe_workspace_size_ex(const moe_cfg* cfg, const moe_options* opts);
+
+/* moe_route with options: valid_mask, aux_kl and aux_std2 apply; n_shared and
+ * activation do not change the routing (they only size the workspace). The
+ * workspace must hold moe_workspace_size_ex(cfg, opts) bytes. Returns MOE_EINVAL
+ * for an out-of-range n_shared or activation. */
+int moe_route_ex(const moe_cfg* cfg, const moe_options* opts, const void* x,
+                 const void* w_router, const float* router_bias, int32_t* topk_idx,
+                 float* topk_w, float* aux_loss, uint8_t* drop_mask,
+                 int32_t* expert_counts, int32_t* kept_counts, void* workspace,
+                 size_t workspace_bytes, void* stream);
+
+/* moe_forward_timed with options (stage_events may be NULL; stage 3 is GEMM1 with
+ * the chosen activation). out[t] = the routed sum as in moe_forward plus the sum of
+ * the n_shared shared experts' outputs; padding tokens get 0. w3 may be NULL with
+ * MOE_ACT_GELU. The workspace must hold moe_workspace_size_ex(cfg, opts) bytes. */
+int moe_forward_ex(const moe_cfg* cfg, const moe_options* opts, const void* x,
+                   const void* w_router, const float* router_bias, const void* w1,
+                   const void* w3, const void* w2, void* out, int32_t* topk_idx,
+                   float* topk_w, float* aux_loss, uint8_t* drop_mask,
+                   int32_t* expert_counts, int32_t* kept_counts, void* workspace,
+                   size_t workspace_bytes, void* stream, void* const* stage_events);
+
 /* Static description of a status code. */
 const char* moe_strerror(int status);
 

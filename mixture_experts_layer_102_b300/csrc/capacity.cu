@@ -8,62 +8,83 @@
 // factor). Kept slots go to row offsets[e] + rank of the permuted buffer ("scatter
 // tokens into expert queues", devpress.csdn.net MoE page section 4.1), copied with
 // 16-byte vectors, one warp per token.
+//
+// Shared experts (hotelren.com/news/5904824 section 3.3) are slots k..k+S-1 of every
+// valid token: row offsets[N+j] + the token's rank among the valid tokens. A padding
+// token (index -1 from the routing decisions) gets no row and every slot dropped.
 #include "common.cuh"
 #include "internal.h"
 
 namespace moe {
 namespace {
 
+constexpr int MAX_SLOTS = 32 + MAX_SHARED;
+
 // One warp per token; a block is 8 tokens.
 template <typename TIn, bool COPY>
 __global__ void __launch_bounds__(256) dispatch_kernel(DispatchArgs a) {
-  __shared__ int32_t rows[8][32];
+  __shared__ int32_t rows[8][MAX_SLOTS];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * 8 + warp;
   pdl_wait();  // ranks, bases and offsets come from the routing-decision kernel
   pdl_trigger();
   if (t >= a.T) return;
-  int row = -1;
-  if (lane < a.k) {
-    const int j = t * a.k + lane;
-    const int e = a.idx[j];
-    if (e < 0 || e >= a.N) {
-      report(a.status, STATUS_BAD_INDEX);
-      a.drop[j] = 1;
-    } else {
-      const long long rank =
-          (long long)a.blk_base[(size_t)(t / a.tokens_per_block) * a.N + e] + a.slot_rank[j];
-      const bool kept = a.C < 0 || rank < a.C;
-      if (kept) {
-        row = a.offsets[e] + (int)rank;
-        if (row >= a.A_cap) {
-          report(a.status, STATUS_BAD_INDEX);
-          row = -1;
-        } else {
-          a.row_token[row] = t;
-        }
-      }
-      a.drop[j] = kept ? 0 : 1;
+  // The token's first VPL x vectors per lane are requested before the chain of
+  // dependent index loads below, so the two overlap.
+  constexpr int VPL = 8;
+  const uint4* src = reinterpret_cast<const uint4*>(static_cast<const TIn*>(a.x) + (size_t)t * a.H);
+  const int nvec = a.H * (int)sizeof(TIn) / 16;
+  uint4 val[VPL];
+  if (COPY) {
+#pragma unroll
+    for (int u = 0; u < VPL; ++u) {
+      const int v = u * 32 + lane;
+      if (v < nvec) val[u] = src[v];
     }
-    a.slot_row[j] = row;
-    rows[warp][lane] = row;
+  }
+  const int slots = a.k + a.S;
+  const long long C = a.valid != nullptr ? (long long)*a.cap : a.C;
+  const int blk = t / a.tokens_per_block;
+  for (int sl = lane; sl < slots; sl += 32) {
+    int row = -1;
+    if (sl < a.k) {  // routed slot
+      const int j = t * a.k + sl;
+      const int e = a.idx[j];
+      if (e < 0 && a.valid != nullptr && a.valid[t] == 0) {
+        a.drop[j] = 1;  // padding token
+      } else if (e < 0 || e >= a.N) {
+        report(a.status, STATUS_BAD_INDEX);
+        a.drop[j] = 1;
+      } else {
+        const long long rank = (long long)a.blk_base[(size_t)blk * a.N + e] + a.slot_rank[j];
+        const bool kept = C < 0 || rank < C;
+        if (kept) row = a.offsets[e] + (int)rank;
+        a.drop[j] = kept ? 0 : 1;
+      }
+    } else if (a.valid == nullptr || a.valid[t] != 0) {  // shared expert N + (sl - k)
+      const int vr = a.valid == nullptr ? t : a.blk_vbase[blk] + a.vrank[t];
+      row = a.offsets[a.N + sl - a.k] + vr;
+    }
+    if (row >= a.A_cap) {
+      report(a.status, STATUS_BAD_INDEX);
+      row = -1;
+    }
+    if (row >= 0) a.row_token[row] = t;
+    a.slot_row[(size_t)t * slots + sl] = row;
+    rows[warp][sl] = row;
   }
   __syncwarp();
   if (COPY) {
-    // Up to VPL 16-byte loads in flight per lane before the k row stores.
-    constexpr int VPL = 8;
-    const uint4* src = reinterpret_cast<const uint4*>(static_cast<const TIn*>(a.x) +
-                                                      (size_t)t * a.H);
     uint4* dst = reinterpret_cast<uint4*>(a.xp);
-    const int nvec = a.H * (int)sizeof(TIn) / 16;
     for (int v0 = 0; v0 < nvec; v0 += 32 * VPL) {
-      uint4 val[VPL];
+      if (v0 > 0) {
 #pragma unroll
-      for (int u = 0; u < VPL; ++u) {
-        const int v = v0 + u * 32 + lane;
-        if (v < nvec) val[u] = src[v];
+        for (int u = 0; u < VPL; ++u) {
+          const int v = v0 + u * 32 + lane;
+          if (v < nvec) val[u] = src[v];
+        }
       }
-      for (int s = 0; s < a.k; ++s) {
+      for (int s = 0; s < slots; ++s) {
         const int r = rows[warp][s];
         if (r < 0) continue;
         uint4* drow = dst + (size_t)r * nvec;

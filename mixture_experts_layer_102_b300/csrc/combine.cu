@@ -4,6 +4,9 @@
 // order). Dropped slots contribute nothing and the kept slots keep their weights;
 // the residual is added by the caller (cf-1.com/news/5914943 section 2.3 note).
 //
+// Shared experts (hotelren.com/news/5904824 section 3.3) are slots k..k+S-1 with
+// weight 1; a padding token has no row in any slot and gets 0.
+//
 // One warp per token, 16-byte vectors, fp32 accumulation in a fixed slot order so
 // the result does not depend on scheduling.
 #include "common.cuh"
@@ -15,17 +18,20 @@ namespace {
 template <typename TIo>
 __global__ void __launch_bounds__(256)
 combine_kernel(const TIo* __restrict__ ye, const int32_t* __restrict__ slot_row,
-               const float* __restrict__ w, int T, int k, int H, TIo* __restrict__ out) {
-  __shared__ int32_t rows[8][32];
-  __shared__ float wts[8][32];
+               const float* __restrict__ w, int T, int k, int S, int H,
+               TIo* __restrict__ out) {
+  constexpr int MAX_SLOTS = 32 + MAX_SHARED;
+  __shared__ int32_t rows[8][MAX_SLOTS];
+  __shared__ float wts[8][MAX_SLOTS];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * 8 + warp;
   pdl_wait();  // ye comes from the second expert GEMM
   pdl_trigger();
   if (t >= T) return;
-  if (lane < k) {
-    rows[warp][lane] = slot_row[(size_t)t * k + lane];
-    wts[warp][lane] = w[(size_t)t * k + lane];
+  const int slots = k + S;
+  for (int sl = lane; sl < slots; sl += 32) {
+    rows[warp][sl] = slot_row[(size_t)t * slots + sl];
+    wts[warp][sl] = sl < k ? w[(size_t)t * k + sl] : 1.f;
   }
   __syncwarp();
   // Groups of 8 elements (one 16-byte bf16 vector); each lane keeps VPL groups in
@@ -38,7 +44,7 @@ combine_kernel(const TIo* __restrict__ ye, const int32_t* __restrict__ slot_row,
     for (int u = 0; u < VPL; ++u)
 #pragma unroll
       for (int q = 0; q < 8; ++q) acc[u][q] = 0.f;
-    for (int s = 0; s < k; ++s) {
+    for (int s = 0; s < slots; ++s) {
       const int r = rows[warp][s];
       if (r < 0) continue;
       const float ws = wts[warp][s];
@@ -69,15 +75,16 @@ combine_kernel(const TIo* __restrict__ ye, const int32_t* __restrict__ slot_row,
 }  // namespace
 
 cudaError_t launch_combine(int dtype, const void* ye, const int32_t* slot_row, const float* w,
-                           int T, int k, int H, void* out, cudaStream_t stream, bool pdl) {
+                           int T, int k, int S, int H, void* out, cudaStream_t stream,
+                           bool pdl) {
   if (T == 0) return cudaSuccess;
   const dim3 grid((T + 7) / 8), block(256);
   if (dtype == 1)
     return launch_kernel(combine_kernel<__nv_bfloat16>, grid, block, 0, stream, pdl,
-                         static_cast<const __nv_bfloat16*>(ye), slot_row, w, T, k, H,
+                         static_cast<const __nv_bfloat16*>(ye), slot_row, w, T, k, S, H,
                          static_cast<__nv_bfloat16*>(out));
   return launch_kernel(combine_kernel<float>, grid, block, 0, stream, pdl,
-                       static_cast<const float*>(ye), slot_row, w, T, k, H,
+                       static_cast<const float*>(ye), slot_row, w, T, k, S, H,
                        static_cast<float*>(out));
 }
 

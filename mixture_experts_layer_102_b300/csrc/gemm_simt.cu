@@ -4,6 +4,7 @@
 // buffer, visited as 128-row tiles from the tile table the capacity scan writes.
 //
 //   swiglu: out = silu(A W1_e^T) * (A W3_e^T)   (2kiu.com/news/2885792 section 2.2)
+//   gelu:   out = gelu(A W1_e^T), exact erf GELU (devpress.csdn.net MoE page section 4.1)
 //   plain:  out = A W2_e^T
 #include "common.cuh"
 #include "internal.h"
@@ -15,12 +16,13 @@ constexpr int BM = TILE_ROWS_1;  // 128 rows: one tile of the 128-row table per 
 constexpr int BN = 64;           // output columns per block
 constexpr int BK = 16;
 
-template <bool SWIGLU>
+template <int EPI>
 __global__ void __launch_bounds__(256)
 gemm_simt_kernel(const float* __restrict__ A, const float* __restrict__ B0,
                  const float* __restrict__ B1, float* __restrict__ out, int K, int n_cols,
                  const int32_t* __restrict__ tile_expert, const int32_t* __restrict__ tile_row0,
                  const int32_t* __restrict__ offsets, const int32_t* __restrict__ num_mtiles) {
+  constexpr bool SWIGLU = EPI == EPI_SWIGLU;
   const int mt = blockIdx.x;
   pdl_wait();
   pdl_trigger();
@@ -80,7 +82,11 @@ gemm_simt_kernel(const float* __restrict__ A, const float* __restrict__ B0,
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const int c = n0 + tx * 4 + j;
-      if (c < n_cols) out[(size_t)r * n_cols + c] = SWIGLU ? silu(acc0[i][j]) * acc1[i][j] : acc0[i][j];
+      if (c >= n_cols) continue;
+      float v = acc0[i][j];
+      if constexpr (EPI == EPI_SWIGLU) v = silu(v) * acc1[i][j];
+      if constexpr (EPI == EPI_GELU) v = 0.5f * v * (1.0f + erff(v * 0.70710678118654752f));
+      out[(size_t)r * n_cols + c] = v;
     }
   }
 }
@@ -90,16 +96,21 @@ gemm_simt_kernel(const float* __restrict__ A, const float* __restrict__ B0,
 cudaError_t launch_grouped_gemm_simt(const GroupedGemmArgs& a, cudaStream_t stream) {
   if (a.max_mtiles == 0) return cudaSuccess;
   const dim3 grid(a.max_mtiles, (a.n_cols + BN - 1) / BN);
-  if (a.swiglu)
-    gemm_simt_kernel<true><<<grid, 256, 0, stream>>>(
-        static_cast<const float*>(a.A), static_cast<const float*>(a.B0),
-        static_cast<const float*>(a.B1), static_cast<float*>(a.out), a.K, a.n_cols,
-        a.tile_expert, a.tile_row0, a.offsets, a.num_mtiles);
+  const float* A = static_cast<const float*>(a.A);
+  const float* B0 = static_cast<const float*>(a.B0);
+  float* out = static_cast<float*>(a.out);
+  if (a.epi == EPI_SWIGLU)
+    gemm_simt_kernel<EPI_SWIGLU><<<grid, 256, 0, stream>>>(
+        A, B0, static_cast<const float*>(a.B1), out, a.K, a.n_cols, a.tile_expert, a.tile_row0,
+        a.offsets, a.num_mtiles);
+  else if (a.epi == EPI_GELU)
+    gemm_simt_kernel<EPI_GELU><<<grid, 256, 0, stream>>>(A, B0, nullptr, out, a.K, a.n_cols,
+                                                         a.tile_expert, a.tile_row0, a.offsets,
+                                                         a.num_mtiles);
   else
-    gemm_simt_kernel<false><<<grid, 256, 0, stream>>>(
-        static_cast<const float*>(a.A), static_cast<const float*>(a.B0), nullptr,
-        static_cast<float*>(a.out), a.K, a.n_cols, a.tile_expert, a.tile_row0, a.offsets,
-        a.num_mtiles);
+    gemm_simt_kernel<EPI_PLAIN><<<grid, 256, 0, stream>>>(A, B0, nullptr, out, a.K, a.n_cols,
+                                                          a.tile_expert, a.tile_row0, a.offsets,
+                                                          a.num_mtiles);
   return cudaGetLastError();
 }
 

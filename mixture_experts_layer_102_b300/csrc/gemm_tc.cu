@@ -6,14 +6,16 @@
 // a static schedule of (expert row tile, column tile) work items:
 //
 //   GEMM1 (swiglu): h[r, n0:n0+128] = silu(xp_r W1_e[n0:n0+128]^T) * (xp_r W3_e[n0:n0+128]^T)
+//   GEMM1 (gelu):   h[r, n0:n0+256] = gelu(xp_r W1_e[n0:n0+256]^T)
+//                   (the two-layer GELU expert, devpress.csdn.net MoE page section 4.1)
 //   GEMM2 (plain):  ye[r, n0:n0+256] = h_r W2_e[n0:n0+256]^T
 //
 // Two tile shapes, one template (CG = CTAs per tile):
 //   CG = 1  one CTA per 128-row tile: tcgen05.mma.cta_group::1, M=128 N=256 K=16;
 //           per stage the CTA stages 128 A rows and a 256-row B tile made of two
 //           128-row boxes (W1 rows n0.. and the matching W3 rows for GEMM1, so gate
-//           and up land side by side in every accumulator row; W2 rows n0.. and
-//           n0+128.. for GEMM2): 4 stages of 48 KB.
+//           and up land side by side in every accumulator row; W1 or W2 rows n0..
+//           and n0+128.. otherwise): 4 stages of 48 KB.
 //   CG = 2  a cluster of two CTAs per 256-row tile: tcgen05.mma.cta_group::2, M=256
 //           N=256 K=16; each CTA stages its own 128 A rows and one 128-row half of B
 //           (the W1 box in the first CTA, the W3 box in the second), both CTAs' loads
@@ -78,6 +80,11 @@ __host__ __device__ constexpr uint32_t idesc() {
 // negative z and the quotient then reads 0, the limit of silu.
 __device__ __forceinline__ float silu_fast(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
 
+// Exact GELU, z * Phi(z) = z/2 * (1 + erf(z / sqrt 2)).
+__device__ __forceinline__ float gelu_erf(float z) {
+  return 0.5f * z * (1.0f + erff(z * 0.70710678118654752f));
+}
+
 // Work item w -> (row tile, column tile). Items are grouped by expert (an expert's
 // tiles x all column tiles, experts in order); inside an expert, bands of GROUP_M row
 // tiles sweep the column tiles with the row tile fastest, so the units in flight share
@@ -119,7 +126,7 @@ struct TcArgs {
   uint32_t* status;
 };
 
-template <bool SWIGLU, int CG>
+template <int EPI, int CG>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                        const __grid_constant__ CUtensorMap tmB0,
@@ -183,7 +190,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
   pdl_wait();  // tile tables and the A rows come from earlier kernels
   pdl_trigger();
 
-  __shared__ int32_t tfirst[257];
+  __shared__ int32_t tfirst[MAX_EXPERTS + 1];
   for (int i = threadIdx.x; i <= a.N; i += blockDim.x) tfirst[i] = a.tile_first[i];
   __syncthreads();
   const int num_mt = *a.num_mtiles;
@@ -316,7 +323,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
       const uint32_t t = tmem_base + lane_addr + (uint32_t)(acc * ACC_COLS);
       __nv_bfloat16* orow = a.out + (size_t)r * a.out_ld + (size_t)nt * a.n_per_tile;
       const int cols_left = a.n_valid - nt * a.n_per_tile;
-      if (SWIGLU) {  // h columns [64*half, 64*half + 64): gate at c, up at 128 + c
+      if constexpr (EPI == EPI_SWIGLU) {  // h columns [64*half, 64*half + 64): gate at c, up at 128 + c
 #pragma unroll 1
         for (int c = 64 * half; c < 64 * half + 64; c += 16) {
           uint32_t g[16], u[16];
@@ -337,7 +344,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
             dst[1] = make_uint4(p[4], p[5], p[6], p[7]);
           }
         }
-      } else {  // ye columns [128*half, 128*half + 128)
+      } else {  // columns [128*half, 128*half + 128) of ye (plain) or h (gelu)
 #pragma unroll 1
         for (int c = 128 * half; c < 128 * half + 128; c += 16) {
           uint32_t v[16];
@@ -346,8 +353,14 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
           if (valid && c < cols_left) {
             uint32_t p[8];
 #pragma unroll
-            for (int q = 0; q < 8; ++q)
-              p[q] = pack_bf16x2(__uint_as_float(v[2 * q]), __uint_as_float(v[2 * q + 1]));
+            for (int q = 0; q < 8; ++q) {
+              float v0 = __uint_as_float(v[2 * q]), v1 = __uint_as_float(v[2 * q + 1]);
+              if constexpr (EPI == EPI_GELU) {
+                v0 = gelu_erf(v0);
+                v1 = gelu_erf(v1);
+              }
+              p[q] = pack_bf16x2(v0, v1);
+            }
             uint4* dst = reinterpret_cast<uint4*>(orow + c);
             dst[0] = make_uint4(p[0], p[1], p[2], p[3]);
             dst[1] = make_uint4(p[4], p[5], p[6], p[7]);
@@ -385,7 +398,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
 // ------------------------------------------------------------------ host side
 
 // Work units (CTAs, or CTA pairs) that can be resident at once: the grid size.
-template <bool SWIGLU, int CG>
+template <int EPI, int CG>
 int grid_units() {
   static int cached[64] = {0};
   int dev = 0;
@@ -407,7 +420,7 @@ int grid_units() {
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
     int c = 0;
-    if (cudaOccupancyMaxActiveClusters(&c, grouped_gemm_tc_kernel<SWIGLU, CG>, &cfg) ==
+    if (cudaOccupancyMaxActiveClusters(&c, grouped_gemm_tc_kernel<EPI, CG>, &cfg) ==
             cudaSuccess &&
         c > 0)
       n = c;
@@ -418,15 +431,15 @@ int grid_units() {
   return n;
 }
 
-template <bool SWIGLU, int CG>
+template <int EPI, int CG>
 cudaError_t launch_t(const CUtensorMap& mA, const CUtensorMap& mB0, const CUtensorMap& mB1,
                      const TcArgs& t, cudaStream_t stream, bool pdl) {
-  cudaError_t e = cudaFuncSetAttribute(grouped_gemm_tc_kernel<SWIGLU, CG>,
+  cudaError_t e = cudaFuncSetAttribute(grouped_gemm_tc_kernel<EPI, CG>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)Shape<CG>::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(CG * grid_units<SWIGLU, CG>(), 1, 1);
+  cfg.gridDim = dim3(CG * grid_units<EPI, CG>(), 1, 1);
   cfg.blockDim = dim3(NUM_THREADS, 1, 1);
   cfg.dynamicSmemBytes = Shape<CG>::SMEM_BYTES;
   cfg.stream = stream;
@@ -446,7 +459,7 @@ cudaError_t launch_t(const CUtensorMap& mA, const CUtensorMap& mB0, const CUtens
   }
   cfg.attrs = attr;
   cfg.numAttrs = n;
-  e = cudaLaunchKernelEx(&cfg, grouped_gemm_tc_kernel<SWIGLU, CG>, mA, mB0, mB1, t);
+  e = cudaLaunchKernelEx(&cfg, grouped_gemm_tc_kernel<EPI, CG>, mA, mB0, mB1, t);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -455,11 +468,13 @@ cudaError_t launch_t(const CUtensorMap& mA, const CUtensorMap& mB0, const CUtens
 
 cudaError_t launch_grouped_gemm_tc(const GroupedGemmArgs& a, cudaStream_t stream, bool pdl) {
   if (a.max_mtiles == 0 || a.A_rows == 0) return cudaSuccess;
+  if (a.N > MAX_EXPERTS) return cudaErrorInvalidValue;
+  const bool swiglu = a.epi == EPI_SWIGLU;
   CUtensorMap mA, mB0, mB1;
   if (!make_map(&mA, a.A, 2, (uint64_t)a.K, 0, (uint64_t)a.A_rows)) return cudaErrorInvalidValue;
   if (!make_map(&mB0, a.B0, 3, (uint64_t)a.K, (uint64_t)a.n_cols, (uint64_t)a.N))
     return cudaErrorInvalidValue;
-  if (!make_map(&mB1, a.swiglu ? a.B1 : a.B0, 3, (uint64_t)a.K, (uint64_t)a.n_cols, (uint64_t)a.N))
+  if (!make_map(&mB1, swiglu ? a.B1 : a.B0, 3, (uint64_t)a.K, (uint64_t)a.n_cols, (uint64_t)a.N))
     return cudaErrorInvalidValue;
   TcArgs t;
   t.tile_expert = a.tile_expert;
@@ -471,16 +486,22 @@ cudaError_t launch_grouped_gemm_tc(const GroupedGemmArgs& a, cudaStream_t stream
   t.out = static_cast<__nv_bfloat16*>(a.out);
   t.out_ld = a.n_cols;
   t.K = a.K;
-  t.n_per_tile = a.swiglu ? 128 : 256;
+  t.n_per_tile = swiglu ? 128 : 256;
   t.n_tiles = (a.n_cols + t.n_per_tile - 1) / t.n_per_tile;
   t.n_valid = a.n_cols;
-  t.b1_row_off = a.swiglu ? 0 : 128;
+  t.b1_row_off = swiglu ? 0 : 128;
   t.status = a.status;
-  if (a.pair)
-    return a.swiglu ? launch_t<true, 2>(mA, mB0, mB1, t, stream, pdl)
-                    : launch_t<false, 2>(mA, mB0, mB1, t, stream, pdl);
-  return a.swiglu ? launch_t<true, 1>(mA, mB0, mB1, t, stream, pdl)
-                  : launch_t<false, 1>(mA, mB0, mB1, t, stream, pdl);
+  switch (a.epi) {
+    case EPI_SWIGLU:
+      return a.pair ? launch_t<EPI_SWIGLU, 2>(mA, mB0, mB1, t, stream, pdl)
+                    : launch_t<EPI_SWIGLU, 1>(mA, mB0, mB1, t, stream, pdl);
+    case EPI_GELU:
+      return a.pair ? launch_t<EPI_GELU, 2>(mA, mB0, mB1, t, stream, pdl)
+                    : launch_t<EPI_GELU, 1>(mA, mB0, mB1, t, stream, pdl);
+    default:
+      return a.pair ? launch_t<EPI_PLAIN, 2>(mA, mB0, mB1, t, stream, pdl)
+                    : launch_t<EPI_PLAIN, 1>(mA, mB0, mB1, t, stream, pdl);
+  }
 }
 
 }  // namespace moe

@@ -14,6 +14,11 @@ constexpr int ROUTER_KC = 32;          // hidden columns per router k-chunk
 constexpr int SELECT_WARPS = 32;       // warps per routing-decision block
 constexpr int TILE_ROWS_1 = 128;       // rows per expert GEMM tile on one CTA
 constexpr int TILE_ROWS_2 = 256;       // rows per expert GEMM tile on a CTA pair
+constexpr int MAX_SHARED = 8;          // always-on experts
+constexpr int MAX_EXPERTS = 256 + MAX_SHARED;
+
+// Expert GEMM epilogues.
+enum Epilogue : int { EPI_PLAIN = 0, EPI_SWIGLU = 1, EPI_GELU = 2 };
 
 // ---------------------------------------------------------------- router
 // Partial logits part[split][t][e] = sum over this split's hidden columns of
@@ -36,6 +41,16 @@ struct SelectArgs {
   int ksplit;
   const float* bias;            // [N] or null
   int T, N, k;
+  int S;                        // always-on experts N..N+S-1 (rows = the valid tokens)
+  const uint8_t* valid;         // [T] 1 = real token, 0 = padding; null = all real
+  int32_t* vrank;               // [T] rank of a valid token among its block's valid tokens
+  int32_t* blk_valid;           // [nblk] valid tokens per block, then exclusive bases
+  float* blk_d2;                // [nblk] sums of (P - 1/N)^2 (only with aux_std2)
+  int32_t* cap;                 // [1] capacity of the call (-1: no limit)
+  long long C;                  // capacity from T (-1: no limit), used without a mask
+  double cf;                    // capacity factor (<= 0: no limit), used with a mask
+  float* aux_kl;                // [1] or null: KL(uniform || f)
+  float* aux_std2;              // [1] or null: unbiased variance of all P
   int tpw;                      // tokens per warp; a block is SELECT_WARPS warps
   int32_t* idx;                 // [T*k] top-k experts
   float* w;                     // [T*k] gate weights
@@ -43,16 +58,15 @@ struct SelectArgs {
   int32_t* blk_counts;          // [nblk][N] counts, then exclusive per-expert bases
   float* blk_psum;              // [nblk][N] sums of P
   unsigned* done;               // completion counter, zero between calls
-  long long C;                  // capacity, < 0 for no limit
-  int32_t* counts;              // [N] slots per expert before capacity
-  int32_t* kept;                // [N] after capacity
-  int32_t* offsets;             // [N+1] first permuted row of each expert
+  int32_t* counts;              // [N+S] slots per expert before capacity
+  int32_t* kept;                // [N+S] after capacity
+  int32_t* offsets;             // [N+S+1] first permuted row of each expert
   // GEMM row-tile tables for 128-row tiles [0] and 256-row tiles [1]: expert and
   // first permuted row of each tile, and the number of tiles
   int32_t* tile_expert[2];
   int32_t* tile_row0[2];
   int32_t* num_mtiles[2];
-  int32_t* tile_first[2];       // [N+1] first tile of each expert (and the total)
+  int32_t* tile_first[2];       // [N+S+1] first tile of each expert (and the total)
   float* aux;                   // [1]
   int32_t* user_counts;         // optional copies for the caller
   int32_t* user_kept;
@@ -67,14 +81,19 @@ struct DispatchArgs {
   const int32_t* slot_rank;     // [T*k] rank within its routing-decision block
   const int32_t* blk_base;      // [nblk][N] per-expert base of every such block
   int tokens_per_block;
-  const int32_t* offsets;       // [N+1]
-  long long C;
+  const int32_t* offsets;       // [N+S+1]
+  const int32_t* cap;           // [1] capacity of the call, read when a mask is given
+  long long C;                  // capacity from T (-1: no limit), used without a mask
   int T, k, N, H;
+  int S;                        // always-on experts
+  const uint8_t* valid;         // [T] or null
+  const int32_t* vrank;         // [T] valid rank inside the routing block (with a mask)
+  const int32_t* blk_vbase;     // [nblk] valid tokens before each routing block
   int A_cap;                    // rows of the permuted buffer
   const void* x;                // [T,H]
   void* xp;                     // [A_cap,H] (may be null when copy is false)
   uint8_t* drop;                // [T*k]
-  int32_t* slot_row;            // [T*k] permuted row of each slot, -1 when dropped
+  int32_t* slot_row;            // [T*(k+S)] permuted row of each slot, -1 when dropped
   int32_t* row_token;           // [A_cap]
   uint32_t* status;
 };
@@ -88,14 +107,15 @@ struct GroupedGemmArgs {
   const void* B0;               // [N, n_cols, K] (W1 or W2)
   const void* B1;               // [N, n_cols, K] (W3) or null
   void* out;                    // [A_cap, n_cols]
-  int K, n_cols, N;
-  bool swiglu;                  // out = silu(A B0^T) * (A B1^T), else A B0^T
+  int K, n_cols, N;             // N: experts in the weight tensors (routed + shared)
+  int epi;                      // Epilogue: SwiGLU out = silu(A B0^T) * (A B1^T),
+                                // GELU out = gelu(A B0^T), plain out = A B0^T
   bool pair;                    // 256-row tiles on CTA pairs (else 128-row tiles)
   const int32_t* tile_expert;   // the table that matches the tile shape
   const int32_t* tile_row0;
   const int32_t* offsets;
   const int32_t* num_mtiles;
-  const int32_t* tile_first;    // [N+1] first tile of each expert in that table
+  const int32_t* tile_first;    // [N+1] first tile of each expert in that table (N as above)
   int max_mtiles;
   uint32_t* status;
 };
@@ -105,7 +125,9 @@ cudaError_t launch_grouped_gemm_simt(const GroupedGemmArgs& a, cudaStream_t stre
 cudaError_t launch_grouped_gemm_tc(const GroupedGemmArgs& a, cudaStream_t stream, bool pdl);
 
 // ---------------------------------------------------------------- combine
+// out[t] = sum over the k routed slots of w * ye[row] plus the S shared slots with
+// weight 1 (slot_row stride k+S, -1 = no row).
 cudaError_t launch_combine(int dtype, const void* ye, const int32_t* slot_row, const float* w,
-                           int T, int k, int H, void* out, cudaStream_t stream, bool pdl);
+                           int T, int k, int S, int H, void* out, cudaStream_t stream, bool pdl);
 
 }  // namespace moe

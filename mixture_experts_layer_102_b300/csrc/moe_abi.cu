@@ -23,11 +23,38 @@ size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// Options of the *_ex entry points, with NULL read as the base layer.
+struct Opts {
+  int S = 0;                          // shared experts
+  int act = MOE_ACT_SWIGLU;
+  const uint8_t* valid = nullptr;     // [T] or null
+  float* aux_kl = nullptr;
+  float* aux_std2 = nullptr;
+};
+
+int read_opts(const moe_options* o, Opts* out) {
+  Opts r;
+  if (o != nullptr) {
+    if (o->n_shared < 0 || o->n_shared > MOE_MAX_SHARED) return MOE_EINVAL;
+    if (o->activation != MOE_ACT_SWIGLU && o->activation != MOE_ACT_GELU) return MOE_EINVAL;
+    r.S = o->n_shared;
+    r.act = o->activation;
+    r.valid = o->valid_mask;
+    r.aux_kl = o->aux_kl;
+    r.aux_std2 = o->aux_std2;
+  }
+  *out = r;
+  return MOE_OK;
+}
+
 struct Plan {
   int T, H, N, k, F, dtype;
-  long long C;            // -1: no limit
+  int S;                  // shared experts (experts N..N+S-1 of the weight tensors)
+  bool masked;            // a valid-token mask is given
+  float cf;               // capacity factor (<= 0: no limit)
+  long long C;            // capacity without a mask, -1: no limit (an upper bound with one)
   int A;                  // T*k routing slots
-  int A_cap;              // rows of the permuted buffers
+  int A_cap;              // rows of the permuted buffers: kept routed slots + S*T
   int ksplit, chunks_per_split;
   int sel_tpw, n_sel_blocks;
   int max_mtiles[2];      // row tiles of 128 and of 256 rows, upper bounds
@@ -36,8 +63,8 @@ struct Plan {
   size_t elem;
   size_t off_wrt, off_part, off_psum, off_blk, off_rank, off_idx, off_w, off_drop, off_counts,
       off_kept, off_offsets, off_tile_e[2], off_tile_r[2], off_tile_f[2], off_nmt, off_aux,
-      off_slot_row,
-      off_row_token, off_xp, off_h, off_ye, total;
+      off_cap, off_bvalid, off_vrank, off_bd2, off_slot_row, off_row_token, off_xp, off_h,
+      off_ye, total;
 };
 
 int check_cfg(const moe_cfg* c) {
@@ -57,14 +84,18 @@ long long capacity_of(const moe_cfg* c) {
   return cap >= slots ? (long long)slots : (long long)cap;  // an expert never holds more
 }
 
-Plan make_plan(const moe_cfg* c) {
+Plan make_plan(const moe_cfg* c, const Opts& o) {
   Plan p;
   memset(&p, 0, sizeof(p));
   p.T = c->T; p.H = c->H; p.N = c->N; p.k = c->k; p.F = c->F; p.dtype = c->dtype;
-  p.C = capacity_of(c);
+  p.S = o.S;
+  p.masked = o.valid != nullptr;
+  p.cf = c->capacity_factor;
+  p.C = capacity_of(c);  // with a mask the call's C (from T_valid <= T) is no larger
   p.A = c->T * c->k;
   long long cap_rows = p.A;
   if (p.C >= 0 && (long long)p.N * p.C < cap_rows) cap_rows = (long long)p.N * p.C;
+  cap_rows += (long long)p.S * p.T;
   p.A_cap = (int)cap_rows;
   p.elem = c->dtype == MOE_BF16 ? 2 : 4;
   // Router split over H: keep about two blocks per SM when T is small.
@@ -85,12 +116,12 @@ Plan make_plan(const moe_cfg* c) {
   // the last block's scan over the blocks stays short
   p.sel_tpw = p.T / (SELECT_WARPS * 600) > 1 ? p.T / (SELECT_WARPS * 600) : 1;
   p.n_sel_blocks = (p.T + SELECT_WARPS * p.sel_tpw - 1) / (SELECT_WARPS * p.sel_tpw);
-  p.max_mtiles[0] = (p.A_cap + TILE_ROWS_1 - 1) / TILE_ROWS_1 + p.N;
-  p.max_mtiles[1] = (p.A_cap + TILE_ROWS_2 - 1) / TILE_ROWS_2 + p.N;
+  p.max_mtiles[0] = (p.A_cap + TILE_ROWS_1 - 1) / TILE_ROWS_1 + p.N + p.S;
+  p.max_mtiles[1] = (p.A_cap + TILE_ROWS_2 - 1) / TILE_ROWS_2 + p.N + p.S;
   // Expert GEMM tile shape from the expected rows per expert: large groups go to
   // CTA pairs (less shared-memory traffic per SM), small ones to single CTAs (less
   // padding of each expert's last tile, more tiles to spread over the SMs).
-  p.pair = (long long)p.T * p.k >= 1024ll * p.N;
+  p.pair = (long long)p.T * (p.k + p.S) >= 1024ll * (p.N + p.S);
   p.pdl = p.dtype == MOE_BF16;
 
   size_t cur = kStatusBytes;
@@ -99,7 +130,7 @@ Plan make_plan(const moe_cfg* c) {
     cur = align_up(cur + (bytes > 0 ? bytes : 1), kAlign);
     return o;
   };
-  const size_t T = p.T, N = p.N, A = p.A, Ac = p.A_cap;
+  const size_t T = p.T, N = p.N, A = p.A, Ac = p.A_cap, NS = (size_t)p.N + p.S;
   p.off_wrt = take(p.dtype == MOE_BF16 ? (size_t)router_tc_npad(p.N) * p.H * 2 : 0);
   p.off_part = take((size_t)p.ksplit * T * N * 4);
   p.off_psum = take((size_t)p.n_sel_blocks * N * 4);
@@ -108,17 +139,21 @@ Plan make_plan(const moe_cfg* c) {
   p.off_idx = take(A * 4);
   p.off_w = take(A * 4);
   p.off_drop = take(A);
-  p.off_counts = take(N * 4);
-  p.off_kept = take(N * 4);
-  p.off_offsets = take((N + 1) * 4);
+  p.off_counts = take(NS * 4);
+  p.off_kept = take(NS * 4);
+  p.off_offsets = take((NS + 1) * 4);
   for (int tb = 0; tb < 2; ++tb) {
     p.off_tile_e[tb] = take((size_t)p.max_mtiles[tb] * 4);
     p.off_tile_r[tb] = take((size_t)p.max_mtiles[tb] * 4);
-    p.off_tile_f[tb] = take((N + 1) * 4);
+    p.off_tile_f[tb] = take((NS + 1) * 4);
   }
   p.off_nmt = take(8);
   p.off_aux = take(4);
-  p.off_slot_row = take(A * 4);
+  p.off_cap = take(4);
+  p.off_bvalid = take((size_t)p.n_sel_blocks * 4);
+  p.off_vrank = take(p.masked && p.S > 0 ? T * 4 : 0);
+  p.off_bd2 = take((size_t)p.n_sel_blocks * 4);
+  p.off_slot_row = take(T * (size_t)(p.k + p.S) * 4);
   p.off_row_token = take(Ac * 4);
   p.off_xp = take(Ac * p.H * p.elem);
   p.off_h = take(Ac * p.F * p.elem);
@@ -156,8 +191,9 @@ struct Outs {
 };
 
 // Shared front half: router, capacity, dispatch. `copy` gathers x into xp.
-int run_route(const Plan& p, const void* x, const void* w_router, const float* bias,
-              const Outs& o, uint8_t* ws, bool copy, cudaStream_t s, cudaEvent_t* ev) {
+int run_route(const Plan& p, const Opts& op, const void* x, const void* w_router,
+              const float* bias, const Outs& o, uint8_t* ws, bool copy, cudaStream_t s,
+              cudaEvent_t* ev) {
   auto rec = [&](int i) {
     if (ev != nullptr) cudaEventRecord(ev[i], s);
   };
@@ -176,6 +212,16 @@ int run_route(const Plan& p, const void* x, const void* w_router, const float* b
   sa.ksplit = p.ksplit;
   sa.bias = bias;
   sa.T = p.T; sa.N = p.N; sa.k = p.k;
+  sa.S = p.S;
+  sa.valid = op.valid;
+  sa.vrank = reinterpret_cast<int32_t*>(ws + p.off_vrank);
+  sa.blk_valid = reinterpret_cast<int32_t*>(ws + p.off_bvalid);
+  sa.blk_d2 = reinterpret_cast<float*>(ws + p.off_bd2);
+  sa.cap = reinterpret_cast<int32_t*>(ws + p.off_cap);
+  sa.C = p.C;
+  sa.cf = (double)p.cf;
+  sa.aux_kl = op.aux_kl;
+  sa.aux_std2 = op.aux_std2;
   sa.tpw = p.sel_tpw;
   sa.idx = o.idx;
   sa.w = o.w;
@@ -183,7 +229,6 @@ int run_route(const Plan& p, const void* x, const void* w_router, const float* b
   sa.blk_counts = reinterpret_cast<int32_t*>(ws + p.off_blk);
   sa.blk_psum = reinterpret_cast<float*>(ws + p.off_psum);
   sa.done = reinterpret_cast<unsigned*>(ws + kDoneOffset);
-  sa.C = p.C;
   sa.counts = reinterpret_cast<int32_t*>(ws + p.off_counts);
   sa.kept = reinterpret_cast<int32_t*>(ws + p.off_kept);
   sa.offsets = reinterpret_cast<int32_t*>(ws + p.off_offsets);
@@ -204,8 +249,13 @@ int run_route(const Plan& p, const void* x, const void* w_router, const float* b
   da.blk_base = sa.blk_counts;
   da.tokens_per_block = SELECT_WARPS * p.sel_tpw;
   da.offsets = sa.offsets;
+  da.cap = sa.cap;
   da.C = p.C;
   da.T = p.T; da.k = p.k; da.N = p.N; da.H = p.H;
+  da.S = p.S;
+  da.valid = op.valid;
+  da.vrank = sa.vrank;
+  da.blk_vbase = sa.blk_valid;
   da.A_cap = p.A_cap;
   da.x = x;
   da.xp = ws + p.off_xp;
@@ -218,8 +268,8 @@ int run_route(const Plan& p, const void* x, const void* w_router, const float* b
   return MOE_OK;
 }
 
-int run_experts(const Plan& p, const void* w1, const void* w3, const void* w2, void* out,
-                const Outs& o, uint8_t* ws, cudaStream_t s, cudaEvent_t* ev) {
+int run_experts(const Plan& p, const Opts& op, const void* w1, const void* w3, const void* w2,
+                void* out, const Outs& o, uint8_t* ws, cudaStream_t s, cudaEvent_t* ev) {
   auto rec = [&](int i) {
     if (ev != nullptr) cudaEventRecord(ev[i], s);
   };
@@ -228,12 +278,12 @@ int run_experts(const Plan& p, const void* w1, const void* w3, const void* w2, v
   g.A = ws + p.off_xp;
   g.A_rows = p.A_cap;
   g.B0 = w1;
-  g.B1 = w3;
+  g.B1 = op.act == MOE_ACT_SWIGLU ? w3 : nullptr;
   g.out = ws + p.off_h;
   g.K = p.H;
   g.n_cols = p.F;
-  g.N = p.N;
-  g.swiglu = true;
+  g.N = p.N + p.S;
+  g.epi = op.act == MOE_ACT_GELU ? EPI_GELU : EPI_SWIGLU;
   // float32 layers run on CUDA cores over the 128-row table
   const int tb = (p.dtype == MOE_BF16 && p.pair) ? 1 : 0;
   g.pair = tb == 1;
@@ -253,13 +303,13 @@ int run_experts(const Plan& p, const void* w1, const void* w3, const void* w2, v
   g.out = ws + p.off_ye;
   g.K = p.F;
   g.n_cols = p.H;
-  g.swiglu = false;
+  g.epi = EPI_PLAIN;
   if (p.dtype == MOE_BF16) MOE_TRY(launch_grouped_gemm_tc(g, s, p.pdl));
   else MOE_TRY(launch_grouped_gemm_simt(g, s));
   rec(5);
   MOE_TRY(launch_combine(p.dtype, ws + p.off_ye,
                          reinterpret_cast<const int32_t*>(ws + p.off_slot_row), o.w, p.T, p.k,
-                         p.H, out, s, p.pdl));
+                         p.S, p.H, out, s, p.pdl));
   rec(6);
   return MOE_OK;
 }
@@ -269,34 +319,50 @@ int check_ws(const Plan& p, void* ws, size_t ws_bytes) {
   return MOE_OK;
 }
 
-// T = 0: nothing to route; the aux loss and the counts are zero.
-int empty_batch(const Plan& p, float* aux, int32_t* counts, int32_t* kept, cudaStream_t s,
-                cudaEvent_t* ev) {
+// Options that fit the layer: slot rows of the shared experts stay within the limit
+// on routing slots.
+int check_opts(const moe_cfg* c, const Opts& o) {
+  if ((long long)c->T * (c->k + o.S) > (1ll << 30)) return MOE_EUNSUPPORTED;
+  return MOE_OK;
+}
+
+// T = 0: nothing to route; the losses and the counts are zero.
+int empty_batch(const Plan& p, const Opts& op, float* aux, int32_t* counts, int32_t* kept,
+                cudaStream_t s, cudaEvent_t* ev) {
   if (ev != nullptr)
     for (int i = 0; i <= MOE_NUM_STAGES; ++i) cudaEventRecord(ev[i], s);
   if (aux != nullptr) MOE_TRY(cudaMemsetAsync(aux, 0, sizeof(float), s));
+  if (op.aux_kl != nullptr) MOE_TRY(cudaMemsetAsync(op.aux_kl, 0, sizeof(float), s));
+  if (op.aux_std2 != nullptr) MOE_TRY(cudaMemsetAsync(op.aux_std2, 0, sizeof(float), s));
   if (counts != nullptr) MOE_TRY(cudaMemsetAsync(counts, 0, p.N * sizeof(int32_t), s));
   if (kept != nullptr) MOE_TRY(cudaMemsetAsync(kept, 0, p.N * sizeof(int32_t), s));
   return MOE_OK;
 }
 
-int forward_impl(const moe_cfg* cfg, const void* x, const void* w_router, const float* bias,
-                 const void* w1, const void* w3, const void* w2, void* out, int32_t* topk_idx,
-                 float* topk_w, float* aux_loss, uint8_t* drop_mask, int32_t* expert_counts,
-                 int32_t* kept_counts, void* workspace, size_t workspace_bytes, void* stream,
+int forward_impl(const moe_cfg* cfg, const moe_options* opts, const void* x,
+                 const void* w_router, const float* bias, const void* w1, const void* w3,
+                 const void* w2, void* out, int32_t* topk_idx, float* topk_w, float* aux_loss,
+                 uint8_t* drop_mask, int32_t* expert_counts, int32_t* kept_counts,
+                 void* workspace, size_t workspace_bytes, void* stream,
                  void* const* stage_events) {
   int rc = check_cfg(cfg);
   if (rc != MOE_OK) return rc;
+  Opts op;
+  rc = read_opts(opts, &op);
+  if (rc != MOE_OK) return rc;
+  rc = check_opts(cfg, op);
+  if (rc != MOE_OK) return rc;
   // x and out hold T rows: with T = 0 they may be NULL (an empty tensor's address).
-  if (w_router == nullptr || w1 == nullptr || w3 == nullptr || w2 == nullptr ||
+  if (w_router == nullptr || w1 == nullptr || w2 == nullptr ||
+      (op.act == MOE_ACT_SWIGLU && w3 == nullptr) ||
       (cfg->T > 0 && (x == nullptr || out == nullptr)))
     return MOE_EINVAL;
   if (!aligned(x, 16) || !aligned(w_router, 16) || !aligned(w1, 16) || !aligned(w3, 16) ||
       !aligned(w2, 16) || !aligned(out, 16) || !aligned(bias, 4) || !aligned(topk_idx, 4) ||
       !aligned(topk_w, 4) || !aligned(aux_loss, 4) || !aligned(expert_counts, 4) ||
-      !aligned(kept_counts, 4))
+      !aligned(kept_counts, 4) || !aligned(op.aux_kl, 4) || !aligned(op.aux_std2, 4))
     return MOE_EALIGN;
-  const Plan p = make_plan(cfg);
+  const Plan p = make_plan(cfg, op);
   rc = check_ws(p, workspace, workspace_bytes);
   if (rc != MOE_OK) return rc;
   rc = device_check();
@@ -305,7 +371,7 @@ int forward_impl(const moe_cfg* cfg, const void* x, const void* w_router, const 
   cudaEvent_t* ev = stage_events ? reinterpret_cast<cudaEvent_t*>(const_cast<void**>(stage_events))
                                  : nullptr;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  if (p.T == 0) return empty_batch(p, aux_loss, expert_counts, kept_counts, s, ev);
+  if (p.T == 0) return empty_batch(p, op, aux_loss, expert_counts, kept_counts, s, ev);
   Outs o;
   o.idx = topk_idx ? topk_idx : reinterpret_cast<int32_t*>(ws + p.off_idx);
   o.w = topk_w ? topk_w : reinterpret_cast<float*>(ws + p.off_w);
@@ -313,9 +379,41 @@ int forward_impl(const moe_cfg* cfg, const void* x, const void* w_router, const 
   o.drop = drop_mask ? drop_mask : ws + p.off_drop;
   o.counts = expert_counts;
   o.kept = kept_counts;
-  rc = run_route(p, x, w_router, bias, o, ws, true, s, ev);
+  rc = run_route(p, op, x, w_router, bias, o, ws, true, s, ev);
   if (rc != MOE_OK) return rc;
-  return run_experts(p, w1, w3, w2, out, o, ws, s, ev);
+  return run_experts(p, op, w1, w3, w2, out, o, ws, s, ev);
+}
+
+int route_impl(const moe_cfg* cfg, const moe_options* opts, const void* x,
+               const void* w_router, const float* router_bias, int32_t* topk_idx,
+               float* topk_w, float* aux_loss, uint8_t* drop_mask, int32_t* expert_counts,
+               int32_t* kept_counts, void* workspace, size_t workspace_bytes, void* stream) {
+  int rc = check_cfg(cfg);
+  if (rc != MOE_OK) return rc;
+  Opts op;
+  rc = read_opts(opts, &op);
+  if (rc != MOE_OK) return rc;
+  rc = check_opts(cfg, op);
+  if (rc != MOE_OK) return rc;
+  if (w_router == nullptr || aux_loss == nullptr ||
+      (cfg->T > 0 && (x == nullptr || topk_idx == nullptr || topk_w == nullptr ||
+                      drop_mask == nullptr)))
+    return MOE_EINVAL;
+  if (!aligned(x, 16) || !aligned(w_router, 16) || !aligned(router_bias, 4) ||
+      !aligned(topk_idx, 4) || !aligned(topk_w, 4) || !aligned(aux_loss, 4) ||
+      !aligned(expert_counts, 4) || !aligned(kept_counts, 4) || !aligned(op.aux_kl, 4) ||
+      !aligned(op.aux_std2, 4))
+    return MOE_EALIGN;
+  const Plan p = make_plan(cfg, op);
+  rc = check_ws(p, workspace, workspace_bytes);
+  if (rc != MOE_OK) return rc;
+  rc = device_check();
+  if (rc != MOE_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  if (p.T == 0) return empty_batch(p, op, aux_loss, expert_counts, kept_counts, s, nullptr);
+  Outs o{topk_idx, topk_w, aux_loss, drop_mask, expert_counts, kept_counts};
+  return run_route(p, op, x, w_router, router_bias, o, ws, false, s, nullptr);
 }
 
 // Routing scratch for callers that cannot allocate device memory (see
@@ -348,9 +446,13 @@ using namespace moe;
 
 extern "C" {
 
-size_t moe_workspace_size(const moe_cfg* cfg) {
+size_t moe_workspace_size(const moe_cfg* cfg) { return moe_workspace_size_ex(cfg, nullptr); }
+
+size_t moe_workspace_size_ex(const moe_cfg* cfg, const moe_options* opts) {
   if (check_cfg(cfg) != MOE_OK) return 0;
-  return make_plan(cfg).total;
+  Opts op;
+  if (read_opts(opts, &op) != MOE_OK || check_opts(cfg, op) != MOE_OK) return 0;
+  return make_plan(cfg, op).total;
 }
 
 int moe_capacity(const moe_cfg* cfg, int64_t* capacity) {
@@ -374,26 +476,16 @@ int moe_route(const moe_cfg* cfg, const void* x, const void* w_router, const flo
               int32_t* topk_idx, float* topk_w, float* aux_loss, uint8_t* drop_mask,
               int32_t* expert_counts, int32_t* kept_counts, void* workspace,
               size_t workspace_bytes, void* stream) {
-  int rc = check_cfg(cfg);
-  if (rc != MOE_OK) return rc;
-  if (w_router == nullptr || aux_loss == nullptr ||
-      (cfg->T > 0 && (x == nullptr || topk_idx == nullptr || topk_w == nullptr ||
-                      drop_mask == nullptr)))
-    return MOE_EINVAL;
-  if (!aligned(x, 16) || !aligned(w_router, 16) || !aligned(router_bias, 4) ||
-      !aligned(topk_idx, 4) || !aligned(topk_w, 4) || !aligned(aux_loss, 4) ||
-      !aligned(expert_counts, 4) || !aligned(kept_counts, 4))
-    return MOE_EALIGN;
-  const Plan p = make_plan(cfg);
-  rc = check_ws(p, workspace, workspace_bytes);
-  if (rc != MOE_OK) return rc;
-  rc = device_check();
-  if (rc != MOE_OK) return rc;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
-  if (p.T == 0) return empty_batch(p, aux_loss, expert_counts, kept_counts, s, nullptr);
-  Outs o{topk_idx, topk_w, aux_loss, drop_mask, expert_counts, kept_counts};
-  return run_route(p, x, w_router, router_bias, o, ws, false, s, nullptr);
+  return route_impl(cfg, nullptr, x, w_router, router_bias, topk_idx, topk_w, aux_loss,
+                    drop_mask, expert_counts, kept_counts, workspace, workspace_bytes, stream);
+}
+
+int moe_route_ex(const moe_cfg* cfg, const moe_options* opts, const void* x,
+                 const void* w_router, const float* router_bias, int32_t* topk_idx,
+                 float* topk_w, float* aux_loss, uint8_t* drop_mask, int32_t* expert_counts,
+                 int32_t* kept_counts, void* workspace, size_t workspace_bytes, void* stream) {
+  return route_impl(cfg, opts, x, w_router, router_bias, topk_idx, topk_w, aux_loss, drop_mask,
+                    expert_counts, kept_counts, workspace, workspace_bytes, stream);
 }
 
 int moe_route_static(const moe_cfg* cfg, const void* x, const void* w_router,
@@ -410,7 +502,8 @@ int moe_route_static(const moe_cfg* cfg, const void* x, const void* w_router,
       !aligned(topk_idx, 4) || !aligned(topk_w, 4) || !aligned(aux_loss, 4) ||
       !aligned(expert_counts, 4) || !aligned(kept_counts, 4))
     return MOE_EALIGN;
-  const Plan p = make_plan(cfg);
+  const Opts op;
+  const Plan p = make_plan(cfg, op);
   // The routing half uses the workspace prefix that ends where the expert buffers
   // begin; it must fit the static array.
   if (p.off_xp > kStaticScratchBytes) return MOE_EUNSUPPORTED;
@@ -422,18 +515,18 @@ int moe_route_static(const moe_cfg* cfg, const void* x, const void* w_router,
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   // The array keeps the previous call's contents: the status word must start at 0.
   MOE_TRY(cudaMemsetAsync(ws, 0, kStatusBytes, s));
-  if (p.T == 0) return empty_batch(p, aux_loss, expert_counts, kept_counts, s, nullptr);
+  if (p.T == 0) return empty_batch(p, op, aux_loss, expert_counts, kept_counts, s, nullptr);
   Outs o{topk_idx, topk_w, aux_loss, drop_mask, expert_counts, kept_counts};
-  return run_route(p, x, w_router, router_bias, o, ws, false, s, nullptr);
+  return run_route(p, op, x, w_router, router_bias, o, ws, false, s, nullptr);
 }
 
 int moe_forward(const moe_cfg* cfg, const void* x, const void* w_router, const float* router_bias,
                 const void* w1, const void* w3, const void* w2, void* out, int32_t* topk_idx,
                 float* topk_w, float* aux_loss, uint8_t* drop_mask, int32_t* expert_counts,
                 int32_t* kept_counts, void* workspace, size_t workspace_bytes, void* stream) {
-  return forward_impl(cfg, x, w_router, router_bias, w1, w3, w2, out, topk_idx, topk_w, aux_loss,
-                      drop_mask, expert_counts, kept_counts, workspace, workspace_bytes, stream,
-                      nullptr);
+  return forward_impl(cfg, nullptr, x, w_router, router_bias, w1, w3, w2, out, topk_idx, topk_w,
+                      aux_loss, drop_mask, expert_counts, kept_counts, workspace,
+                      workspace_bytes, stream, nullptr);
 }
 
 int moe_forward_timed(const moe_cfg* cfg, const void* x, const void* w_router,
@@ -442,9 +535,20 @@ int moe_forward_timed(const moe_cfg* cfg, const void* x, const void* w_router,
                       uint8_t* drop_mask, int32_t* expert_counts, int32_t* kept_counts,
                       void* workspace, size_t workspace_bytes, void* stream,
                       void* const* stage_events) {
-  return forward_impl(cfg, x, w_router, router_bias, w1, w3, w2, out, topk_idx, topk_w, aux_loss,
-                      drop_mask, expert_counts, kept_counts, workspace, workspace_bytes, stream,
-                      stage_events);
+  return forward_impl(cfg, nullptr, x, w_router, router_bias, w1, w3, w2, out, topk_idx, topk_w,
+                      aux_loss, drop_mask, expert_counts, kept_counts, workspace,
+                      workspace_bytes, stream, stage_events);
+}
+
+int moe_forward_ex(const moe_cfg* cfg, const moe_options* opts, const void* x,
+                   const void* w_router, const float* router_bias, const void* w1,
+                   const void* w3, const void* w2, void* out, int32_t* topk_idx, float* topk_w,
+                   float* aux_loss, uint8_t* drop_mask, int32_t* expert_counts,
+                   int32_t* kept_counts, void* workspace, size_t workspace_bytes, void* stream,
+                   void* const* stage_events) {
+  return forward_impl(cfg, opts, x, w_router, router_bias, w1, w3, w2, out, topk_idx, topk_w,
+                      aux_loss, drop_mask, expert_counts, kept_counts, workspace,
+                      workspace_bytes, stream, stage_events);
 }
 
 int moe_get_status(void* workspace, size_t workspace_bytes, void* stream, uint32_t* bits) {

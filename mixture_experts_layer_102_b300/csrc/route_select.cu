@@ -25,6 +25,19 @@
 // the per-block counts of every expert into per-block bases, and writes the totals,
 // kept = min(count, C), the expert offsets, the GEMM row-tile tables and the aux loss;
 // it then resets the counter for the next call.
+//
+// Options. A valid-token mask (devpress.csdn.net MoE page section 5.2: capacity counts
+// only the non-padding tokens) routes the valid tokens as a batch of their own: a
+// padding token gets no expert (index -1, weight 0), adds nothing to the counts or the
+// probability sums, and T_valid replaces T in C and in the losses; every valid token
+// gets its rank among the valid tokens (per-warp counts, a prefix over the warps, and
+// per-block bases from the last block). Shared experts (hotelren.com/news/5904824
+// section 3.3) are appended to the expert list as experts N..N+S-1 that keep all
+// T_valid tokens, so the offsets and tile tables cover them too. Two more balance
+// losses: KL(uniform || f), f_e = counts_e / (T_valid*k) (hotelren.com/news/3071227
+// section 4.2), and the unbiased variance of all router probabilities
+// (2kiu.com/news/2885792 section 5.1), from per-block sums of (P - 1/N)^2 (the
+// probabilities of a token sum to 1, so their mean is 1/N).
 #include <math.h>
 
 #include "common.cuh"
@@ -46,6 +59,50 @@ __device__ __forceinline__ float warp_sum(float v) {
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
   return v;
 }
+__device__ __forceinline__ double warp_sum(double v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// Exclusive prefix of v over the 1024 threads of the block, in thread order; *total
+// gets the sum. s_w: 32 ints of shared memory. Contains __syncthreads.
+__device__ int block_exclusive_scan(int v, int32_t* s_w, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, d);
+    if (lane >= d) x += y;
+  }
+  if (lane == 31) s_w[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int w = s_w[lane];
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, w, d);
+      if (lane >= d) w += y;
+    }
+    s_w[lane] = w;
+  }
+  __syncthreads();
+  const int before = (warp > 0 ? s_w[warp - 1] : 0) + x - v;
+  *total = s_w[31];
+  __syncthreads();
+  return before;
+}
+
+// Sum of v over the block in a fixed order (deterministic). s_d: 32 doubles.
+__device__ double block_sum(double v, double* s_d) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  v = warp_sum(v);
+  if (lane == 0) s_d[warp] = v;
+  __syncthreads();
+  double r = warp_sum(lane < 32 ? s_d[lane] : 0.0);
+  __syncthreads();
+  return r;
+}
 
 // The last block's scan (1024 threads). Thread (g, col) walks a contiguous range of
 // block rows of one expert column; a warp covers consecutive columns of the same rows,
@@ -54,10 +111,50 @@ __device__ __forceinline__ float warp_sum(float v) {
 __device__ void finish_routing(const SelectArgs& a, int nblk) {
   __shared__ int32_t ip[1024];
   __shared__ float fq[1024];
-  __shared__ int32_t s_counts[256], s_kept[256], s_off[257], s_tile0[2][257];
+  __shared__ int32_t s_counts[MAX_EXPERTS], s_kept[MAX_EXPERTS], s_off[MAX_EXPERTS + 1],
+      s_tile0[2][MAX_EXPERTS + 1];
   __shared__ float s_psum[256];
+  __shared__ int32_t s_w[32];
+  __shared__ double s_d[32];
   const int tid = threadIdx.x;
-  const int N = a.N;
+  const int N = a.N, Ntot = a.N + a.S;
+  // Valid tokens: per-block counts -> exclusive bases, and their total.
+  int T_valid = a.T;
+  if (a.valid != nullptr) {
+    const int R = (nblk + 1023) / 1024;
+    const int b0 = min(nblk, tid * R), b1 = min(nblk, b0 + R);
+    int mine = 0;
+    for (int b = b0; b < b1; ++b) mine += a.blk_valid[b];
+    int run = block_exclusive_scan(mine, s_w, &T_valid);
+    for (int b = b0; b < b1; ++b) {
+      const int c = a.blk_valid[b];
+      a.blk_valid[b] = run;
+      run += c;
+    }
+  }
+  // Capacity of this call: C = ceil(CF * T_valid * k / N) in double, at most T_valid*k
+  // (the host's value when every token is valid). One thread evaluates it (fp64 is
+  // slow on this part) and shares it; the first read comes after the barrier that
+  // follows the column sums below.
+  __shared__ long long s_C;
+  if (tid == 0) {
+    long long C = a.C;
+    if (a.valid != nullptr && a.cf > 0.0) {
+      const double c = ceil(a.cf * (double)T_valid * (double)a.k / (double)N);
+      const double slots = (double)T_valid * (double)a.k;
+      C = c >= slots ? (long long)slots : (long long)c;
+    }
+    s_C = C;
+    *a.cap = (int32_t)C;
+  }
+  double d2 = 0.0;  // sum of (P - 1/N)^2 over the valid tokens
+  if (a.aux_std2 != nullptr) {
+    const int R = (nblk + 1023) / 1024;
+    const int b0 = min(nblk, tid * R), b1 = min(nblk, b0 + R);
+    double mine = 0.0;
+    for (int b = b0; b < b1; ++b) mine += (double)a.blk_d2[b];
+    d2 = block_sum(mine, s_d);
+  }
   int np2 = 1;
   while (np2 < N) np2 <<= 1;
   const int G = 1024 / np2;                 // row groups
@@ -96,9 +193,10 @@ __device__ void finish_routing(const SelectArgs& a, int nblk) {
     fq[tid] += fv;
     __syncthreads();
   }
+  const long long C = s_C;
   if (col < N && g == G - 1) {
     const int run = ip[tid];
-    const int kept = (a.C < 0 || (long long)run <= a.C) ? run : (int)a.C;
+    const int kept = (C < 0 || (long long)run <= C) ? run : (int)C;
     s_counts[col] = run;
     s_kept[col] = kept;
     s_psum[col] = fq[tid];
@@ -106,6 +204,12 @@ __device__ void finish_routing(const SelectArgs& a, int nblk) {
     a.kept[col] = kept;
     if (a.user_counts != nullptr) a.user_counts[col] = run;
     if (a.user_kept != nullptr) a.user_kept[col] = kept;
+  }
+  if (tid < a.S) {  // shared experts take every valid token, no capacity
+    s_counts[N + tid] = T_valid;
+    s_kept[N + tid] = T_valid;
+    a.counts[N + tid] = T_valid;
+    a.kept[N + tid] = T_valid;
   }
   if (col < N) {  // exclusive per-expert base of every block
     int run = ip[tid] - isum;
@@ -122,17 +226,25 @@ __device__ void finish_routing(const SelectArgs& a, int nblk) {
     }
   }
   __syncthreads();
-  if (tid < 32) {  // warp 0: offsets, tile starts and the aux loss over the experts
+  if (tid < 32) {  // warp 0: offsets, tile starts and the losses over the experts
     const int lane = tid;
-    const int per = (N + 31) / 32;  // experts per lane, <= 8
-    const int e0 = min(N, lane * per), e1 = min(N, e0 + per);
+    const int per = (Ntot + 31) / 32;  // experts per lane, <= 9
+    const int e0 = min(Ntot, lane * per), e1 = min(Ntot, e0 + per);
     int off = 0, t1 = 0, t2 = 0;
     float fp = 0.f;
+    double lsum = 0.0;
+    int empty = 0;
     for (int e = e0; e < e1; ++e) {
       off += s_kept[e];
       t1 += (s_kept[e] + TILE_ROWS_1 - 1) / TILE_ROWS_1;
       t2 += (s_kept[e] + TILE_ROWS_2 - 1) / TILE_ROWS_2;
-      fp = fmaf((float)s_counts[e], s_psum[e], fp);
+      if (e < N) {
+        fp = fmaf((float)s_counts[e], s_psum[e], fp);
+        if (a.aux_kl != nullptr) {
+          if (s_counts[e] == 0) empty = 1;
+          else lsum += log((double)N * (double)s_counts[e] / ((double)T_valid * (double)a.k));
+        }
+      }
     }
     int xo = off, x1 = t1, x2 = t2;  // inclusive scans over the lanes
 #pragma unroll
@@ -160,19 +272,30 @@ __device__ void finish_routing(const SelectArgs& a, int nblk) {
     }
 #pragma unroll
     for (int d = 16; d > 0; d >>= 1) fp += __shfl_xor_sync(0xffffffffu, fp, d);
+    if (a.aux_kl != nullptr) {
+      lsum = warp_sum(lsum);
+      empty = __any_sync(0xffffffffu, empty);
+    }
     if (lane == 31) {
-      s_off[N] = xo;
-      s_tile0[0][N] = x1;
-      s_tile0[1][N] = x2;
-      a.offsets[N] = xo;
-      a.tile_first[0][N] = x1;
-      a.tile_first[1][N] = x2;
+      s_off[Ntot] = xo;
+      s_tile0[0][Ntot] = x1;
+      s_tile0[1][Ntot] = x2;
+      a.offsets[Ntot] = xo;
+      a.tile_first[0][Ntot] = x1;
+      a.tile_first[1][Ntot] = x2;
       *a.num_mtiles[0] = x1;
       *a.num_mtiles[1] = x2;
-      // aux = N * sum_e (counts_e / (T*k)) * (Psum_e / T); counts <= T*k and
-      // sum_e Psum_e = T keep every term well inside fp32 range
-      const float Tf = (float)a.T;
-      *a.aux = a.T > 0 ? (float)N * (fp / (Tf * (float)a.k)) / Tf : 0.f;
+      // aux = N * sum_e (counts_e / (T*k)) * (Psum_e / T), T the valid tokens;
+      // counts <= T*k and sum_e Psum_e = T keep every term well inside fp32 range
+      const float Tf = (float)T_valid;
+      *a.aux = T_valid > 0 ? (float)N * (fp / (Tf * (float)a.k)) / Tf : 0.f;
+      // KL(uniform || f) = -(1/N) sum_e log(N f_e); +inf when an expert got nothing
+      if (a.aux_kl != nullptr)
+        *a.aux_kl = T_valid == 0 ? 0.f : empty ? INFINITY : (float)(-lsum / (double)N);
+      // unbiased variance of the T_valid*N probabilities around their mean 1/N
+      if (a.aux_std2 != nullptr)
+        *a.aux_std2 =
+            T_valid == 0 ? 0.f : (float)(d2 / ((double)T_valid * (double)N - 1.0));
     }
   }
   __syncthreads();
@@ -180,9 +303,9 @@ __device__ void finish_routing(const SelectArgs& a, int nblk) {
   for (int tb = 0; tb < 2; ++tb) {
     const int rows = tb == 0 ? TILE_ROWS_1 : TILE_ROWS_2;
     const int32_t* t0 = s_tile0[tb];
-    const int total = t0[N];
+    const int total = t0[Ntot];
     for (int i = tid; i < total; i += 1024) {
-      int lo = 0, hi = N - 1;  // last expert with t0[e] <= i
+      int lo = 0, hi = Ntot - 1;  // last expert with t0[e] <= i
       while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
         if (t0[mid] <= i) lo = mid; else hi = mid - 1;
@@ -193,29 +316,73 @@ __device__ void finish_routing(const SelectArgs& a, int nblk) {
   }
 }
 
+// OPT: the valid-token mask or the variance loss may be in use (read at run time);
+// without it those branches are compiled out of the base layer's kernel.
+template <bool OPT>
 __global__ void __launch_bounds__(1024) route_select_kernel(SelectArgs a) {
   extern __shared__ int32_t dyn[];
   int32_t* cnt = dyn;                                   // [WARPS][N] running counts
   float* pw = reinterpret_cast<float*>(dyn + WARPS * a.N);  // [WARPS][N] sums of P
   __shared__ int is_last;
+  __shared__ int32_t s_vbase[WARPS];   // valid tokens before each warp's range
+  __shared__ float s_d2[WARPS];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int N = a.N, k = a.k;
   for (int i = threadIdx.x; i < WARPS * N; i += blockDim.x) {
     cnt[i] = 0;
     pw[i] = 0.f;
   }
-  __syncthreads();
   pdl_wait();  // partial logits come from the router kernel
   pdl_trigger();
   const int NI = (N + 31) >> 5;  // experts per lane, <= 8
   const int tbase = (blockIdx.x * WARPS + warp) * a.tpw;
+  const bool masked = OPT && a.valid != nullptr;
+  if (masked) {  // valid tokens of every warp's range -> warp bases and the block count
+    int nv = 0;
+    for (int i0 = 0; i0 < a.tpw; i0 += 32) {
+      const int t = tbase + i0 + lane;
+      const bool v = i0 + lane < a.tpw && t < a.T && a.valid[t] != 0;
+      nv += __popc(__ballot_sync(0xffffffffu, v));
+    }
+    if (lane == 0) s_vbase[warp] = nv;
+  }
+  if (OPT) __syncthreads();
+  if (masked && warp == 0) {
+    const int c = s_vbase[lane];
+    int x = c;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, d);
+      if (lane >= d) x += y;
+    }
+    s_vbase[lane] = x - c;
+    if (lane == 31) a.blk_valid[blockIdx.x] = x;
+  }
+  __syncthreads();
+  const bool want_d2 = OPT && a.aux_std2 != nullptr;
+  const float invN = 1.f / (float)N;
+  float d2 = 0.f;
+  int vnext = masked ? s_vbase[warp] : 0;
   // warp-local rank and expert of this lane's slot for the first MAX_TPW tokens
   int rank_i[MAX_TPW], exp_i[MAX_TPW];
+  uint32_t live_bits = 0;
 #pragma unroll
   for (int u = 0; u < MAX_TPW; ++u) rank_i[u] = exp_i[u] = 0;
   for (int i = 0; i < a.tpw; ++i) {
     const int t = tbase + i;
     if (t >= a.T) break;
+    if (masked && a.valid[t] == 0) {  // padding: no expert, weight 0, no statistics
+      if (lane < k) {
+        a.idx[(size_t)t * k + lane] = -1;
+        a.w[(size_t)t * k + lane] = 0.f;
+      }
+      continue;
+    }
+    if (i < MAX_TPW) live_bits |= 1u << i;
+    if (masked) {
+      if (a.S > 0 && lane == 0) a.vrank[t] = vnext;
+      ++vnext;
+    }
     float v[8];
 #pragma unroll
     for (int q = 0; q < 8; ++q) v[q] = (q < NI && lane + 32 * q < N) ? 0.f : -INFINITY;
@@ -249,7 +416,11 @@ __global__ void __launch_bounds__(1024) route_select_kernel(SelectArgs a) {
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
       const int e = lane + 32 * q;
-      if (q < NI && e < N) pw[warp * N + e] += ex[q] * inv;
+      if (q < NI && e < N) {
+        const float pe = ex[q] * inv;
+        pw[warp * N + e] += pe;
+        if (want_d2) d2 = fmaf(pe - invN, pe - invN, d2);
+      }
     }
     // top-k: k rounds of a warp arg-max on (logit desc, expert id asc)
     uint32_t taken = 0;
@@ -304,6 +475,10 @@ __global__ void __launch_bounds__(1024) route_select_kernel(SelectArgs a) {
     }
     __syncwarp();
   }
+  if (want_d2) {
+    d2 = warp_sum(d2);
+    if (lane == 0) s_d2[warp] = d2;
+  }
   __syncthreads();
   // exclusive prefix of the counters over the warps: the block's per-expert offsets
   for (int e = threadIdx.x; e < N; e += blockDim.x) {
@@ -318,6 +493,11 @@ __global__ void __launch_bounds__(1024) route_select_kernel(SelectArgs a) {
     a.blk_counts[(size_t)blockIdx.x * N + e] = run;
     a.blk_psum[(size_t)blockIdx.x * N + e] = ps;
   }
+  if (want_d2 && threadIdx.x == 0) {
+    float s2 = 0.f;
+    for (int w = 0; w < WARPS; ++w) s2 += s_d2[w];
+    a.blk_d2[blockIdx.x] = s2;
+  }
   __syncthreads();
   for (int i = 0; i < a.tpw; ++i) {  // warp-local ranks -> in-block ranks
     const int t = tbase + i;
@@ -325,11 +505,14 @@ __global__ void __launch_bounds__(1024) route_select_kernel(SelectArgs a) {
     if (lane < k) {
       const size_t j = (size_t)t * k + lane;
       if (i < MAX_TPW) {
+        if (!OPT || ((live_bits >> i) & 1u)) {
 #pragma unroll
-        for (int u = 0; u < MAX_TPW; ++u)  // static indexing keeps the arrays in registers
-          if (u == i) a.slot_rank[j] = rank_i[u] + cnt[warp * N + exp_i[u]];
+          for (int u = 0; u < MAX_TPW; ++u)  // static indexing keeps the arrays in registers
+            if (u == i) a.slot_rank[j] = rank_i[u] + cnt[warp * N + exp_i[u]];
+        }
       } else {
-        a.slot_rank[j] += cnt[warp * N + a.idx[j]];
+        const int e = a.idx[j];
+        if (!OPT || e >= 0) a.slot_rank[j] += cnt[warp * N + e];
       }
     }
   }
@@ -349,10 +532,12 @@ __global__ void __launch_bounds__(1024) route_select_kernel(SelectArgs a) {
 cudaError_t launch_route_select(const SelectArgs& a, int nblk, cudaStream_t stream, bool pdl) {
   if (a.T == 0) return cudaSuccess;
   const size_t smem = (size_t)WARPS * a.N * 8;  // counters and P sums of every warp
-  const cudaError_t e = cudaFuncSetAttribute(
-      route_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  const bool opt = a.valid != nullptr || a.aux_std2 != nullptr;
+  auto kernel = opt ? route_select_kernel<true> : route_select_kernel<false>;
+  const cudaError_t e =
+      cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  return launch_kernel(route_select_kernel, dim3(nblk), dim3(WARPS * 32), smem, stream, pdl, a);
+  return launch_kernel(kernel, dim3(nblk), dim3(WARPS * 32), smem, stream, pdl, a);
 }
 
 }  // namespace moe

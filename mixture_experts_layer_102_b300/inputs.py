@@ -10,6 +10,11 @@ the order x, router weight, router bias, W1, W3, W2):
 * W2[N,H,F] ~ N(0, 1/F)                            (std = fan_in**-0.5, fan_in = F)
 * optional router bias b[N] = 2.0 * r**-1.1 with r a seeded permutation of 1..N, so
   the hottest expert gets exactly +2.0 (a Zipf(1.1) profile scaled to 2.0 max).
+* with ``n_shared`` shared experts the expert tensors hold N + n_shared experts drawn
+  from the same streams (the first N are the routed experts' weights unchanged).
+* a valid-token mask (``make_valid_mask``): the batch is cut into sequences of
+  ``seq_len`` tokens; sequence b keeps its first L_b tokens, L_b uniform on
+  [0, seq_len], and the rest is padding.
 
 Values are drawn as float32 normals. For bf16 workloads every tensor except the
 bias is rounded to bf16 (round to nearest even) and the rounded values are what both
@@ -88,9 +93,21 @@ def make_x(cfg: MoEConfig, rank: int = 0) -> np.ndarray:
     return _store(_normal(seq, (cfg.T, cfg.H), 1.0), cfg.dtype)
 
 
-def make_inputs(cfg: MoEConfig, rank: int = 0, with_experts: bool = True) -> MoEInputs:
+def make_valid_mask(T: int, seq_len: int, seed: int) -> np.ndarray:
+    """[T] uint8, 1 for real tokens: padded sequences of ``seq_len`` tokens."""
+    g = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, 2000])))
+    n_seq = -(-T // seq_len) if T else 0
+    lengths = g.integers(0, seq_len + 1, size=n_seq)
+    pos = np.arange(T) % seq_len
+    return (pos < lengths[np.arange(T) // seq_len]).astype(np.uint8) if T else \
+        np.zeros(0, np.uint8)
+
+
+def make_inputs(cfg: MoEConfig, rank: int = 0, with_experts: bool = True,
+                n_shared: int = 0) -> MoEInputs:
     seqs = np.random.SeedSequence(cfg.seed).spawn(6)
     T, H, N, F = cfg.T, cfg.H, cfg.N, cfg.F
+    NE = N + n_shared
     x = make_x(cfg, rank)
     w_router = _store(_normal(seqs[1], (H, N), 0.02), cfg.dtype)
     bias = None
@@ -99,9 +116,9 @@ def make_inputs(cfg: MoEConfig, rank: int = 0, with_experts: bool = True) -> MoE
         r = g.permutation(N).astype(np.float64) + 1.0
         bias = (2.0 * r ** -1.1).astype(np.float32)
     if with_experts:
-        w1 = _store(_normal(seqs[3], (N, F, H), H ** -0.5), cfg.dtype)
-        w3 = _store(_normal(seqs[4], (N, F, H), H ** -0.5), cfg.dtype)
-        w2 = _store(_normal(seqs[5], (N, H, F), F ** -0.5), cfg.dtype)
+        w1 = _store(_normal(seqs[3], (NE, F, H), H ** -0.5), cfg.dtype)
+        w3 = _store(_normal(seqs[4], (NE, F, H), H ** -0.5), cfg.dtype)
+        w2 = _store(_normal(seqs[5], (NE, H, F), F ** -0.5), cfg.dtype)
     else:
         w1 = w3 = w2 = None
     return MoEInputs(cfg.dtype, x, w_router, bias, w1, w3, w2)

@@ -21,6 +21,8 @@ LIB_PATH = os.path.join(_HERE, "libmoe_b300.so")
 MOE_OK, MOE_EINVAL, MOE_EUNSUPPORTED, MOE_EWORKSPACE, MOE_EALIGN = 0, 1, 2, 3, 4
 MOE_ECUDA, MOE_EDEVICE, MOE_ENODEVICE = 5, 6, 7
 MOE_F32, MOE_BF16 = 0, 1
+MOE_ACT_SWIGLU, MOE_ACT_GELU = 0, 1
+MOE_MAX_SHARED = 8
 MOE_NUM_STAGES = 6
 STAGE_NAMES = ["router_logits", "route_select", "dispatch", "gemm1_swiglu", "gemm2", "combine"]
 
@@ -35,6 +37,9 @@ _SIGNATURES = {
     "moe_forward_timed": (ctypes.c_int, [_P] + [_P] * 13 + [_P, ctypes.c_size_t, _P, _P]),
     "moe_get_status": (ctypes.c_int, [_P, ctypes.c_size_t, _P, ctypes.POINTER(ctypes.c_uint32)]),
     "moe_route_static": (ctypes.c_int, [_P] + [_P] * 9 + [_P]),
+    "moe_workspace_size_ex": (ctypes.c_size_t, [_P, _P]),
+    "moe_route_ex": (ctypes.c_int, [_P, _P] + [_P] * 9 + [_P, ctypes.c_size_t, _P]),
+    "moe_forward_ex": (ctypes.c_int, [_P, _P] + [_P] * 13 + [_P, ctypes.c_size_t, _P, _P]),
     "moe_strerror": (ctypes.c_char_p, [ctypes.c_int]),
 }
 
@@ -43,6 +48,43 @@ class MoECfg(ctypes.Structure):
     _fields_ = [("T", ctypes.c_int32), ("H", ctypes.c_int32), ("N", ctypes.c_int32),
                 ("k", ctypes.c_int32), ("F", ctypes.c_int32),
                 ("capacity_factor", ctypes.c_float), ("dtype", ctypes.c_int32)]
+
+
+class MoEOptions(ctypes.Structure):
+    _fields_ = [("n_shared", ctypes.c_int32), ("activation", ctypes.c_int32),
+                ("valid_mask", ctypes.c_void_p), ("aux_kl", ctypes.c_void_p),
+                ("aux_std2", ctypes.c_void_p)]
+
+
+@dataclass
+class Options:
+    """The layer variants of moe_options: shared experts, the GELU expert, a
+    valid-token mask ([T] uint8 or bool on the device) and the two extra balance
+    losses (pass [1] float32 device tensors to receive them)."""
+    n_shared: int = 0
+    activation: str = "swiglu"
+    valid_mask: Optional[torch.Tensor] = None
+    aux_kl: Optional[torch.Tensor] = None
+    aux_std2: Optional[torch.Tensor] = None
+
+    def to_c(self) -> MoEOptions:
+        if self.activation not in ("swiglu", "gelu"):
+            raise ValueError(f"activation must be 'swiglu' or 'gelu', got {self.activation!r}")
+        return MoEOptions(int(self.n_shared),
+                          MOE_ACT_GELU if self.activation == "gelu" else MOE_ACT_SWIGLU,
+                          _ptr(self.valid_mask), _ptr(self.aux_kl), _ptr(self.aux_std2))
+
+    def check(self, T: int):
+        if self.valid_mask is not None:
+            if self.valid_mask.dtype not in (torch.uint8, torch.bool):
+                raise ValueError("valid_mask must be uint8 or bool")
+            if not self.valid_mask.is_cuda or tuple(self.valid_mask.shape) != (T,) \
+                    or not self.valid_mask.is_contiguous():
+                raise ValueError(f"valid_mask must be a contiguous CUDA tensor of shape ({T},)")
+        for name in ("aux_kl", "aux_std2"):
+            t = getattr(self, name)
+            if t is not None:
+                _check(t, name, (1,), torch.float32)
 
 
 class MoEError(RuntimeError):
@@ -87,8 +129,11 @@ def cfg_from(config, T: Optional[int] = None) -> MoECfg:
                     config.capacity_factor, config.dtype)
 
 
-def workspace_size(cfg: MoECfg) -> int:
-    n = library().moe_workspace_size(ctypes.byref(cfg))
+def workspace_size(cfg: MoECfg, options: Optional[Options] = None) -> int:
+    if options is None:
+        n = library().moe_workspace_size(ctypes.byref(cfg))
+    else:
+        n = library().moe_workspace_size_ex(ctypes.byref(cfg), ctypes.byref(options.to_c()))
     if n == 0:
         raise MoEError("moe_workspace_size", MOE_EINVAL)
     return int(n)
@@ -112,9 +157,9 @@ def _stream(stream) -> int:
     return stream.cuda_stream
 
 
-def make_workspace(cfg: MoECfg, device=None) -> torch.Tensor:
+def make_workspace(cfg: MoECfg, device=None, options: Optional[Options] = None) -> torch.Tensor:
     """A zeroed device workspace for `cfg` (the library allocates nothing itself)."""
-    n = workspace_size(cfg)
+    n = workspace_size(cfg, options)
     return torch.zeros(n, dtype=torch.uint8, device=device or "cuda")
 
 
@@ -155,20 +200,26 @@ def _routing_outputs(cfg: MoECfg, device) -> Routing:
 
 def route(cfg: MoECfg, x: torch.Tensor, w_router: torch.Tensor,
           router_bias: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
-          stream=None) -> Routing:
-    """moe_route: top-k indices and weights, aux loss, capacity drop mask, counts."""
+          stream=None, options: Optional[Options] = None) -> Routing:
+    """moe_route (moe_route_ex with `options`): top-k indices and weights, aux loss,
+    capacity drop mask, counts."""
     dt = _io_dtype(cfg)
     _check(x, "x", (cfg.T, cfg.H), dt)
     _check(w_router, "w_router", (cfg.H, cfg.N), dt)
     if router_bias is not None:
         _check(router_bias, "router_bias", (cfg.N,), torch.float32)
+    if options is not None:
+        options.check(cfg.T)
     if workspace is None:
-        workspace = make_workspace(cfg, x.device)
+        workspace = make_workspace(cfg, x.device, options)
     r = _routing_outputs(cfg, x.device)
-    rc = library().moe_route(ctypes.byref(cfg), _ptr(x), _ptr(w_router), _ptr(router_bias),
-                             _ptr(r.topk_idx), _ptr(r.topk_w), _ptr(r.aux_loss),
-                             _ptr(r.drop_mask), _ptr(r.expert_counts), _ptr(r.kept_counts),
-                             _ptr(workspace), workspace.numel(), _stream(stream))
+    args = [_ptr(x), _ptr(w_router), _ptr(router_bias), _ptr(r.topk_idx), _ptr(r.topk_w),
+            _ptr(r.aux_loss), _ptr(r.drop_mask), _ptr(r.expert_counts), _ptr(r.kept_counts),
+            _ptr(workspace), workspace.numel(), _stream(stream)]
+    if options is None:
+        rc = library().moe_route(ctypes.byref(cfg), *args)
+    else:
+        rc = library().moe_route_ex(ctypes.byref(cfg), ctypes.byref(options.to_c()), *args)
     if rc != MOE_OK:
         raise MoEError("moe_route", rc)
     return r
@@ -178,39 +229,50 @@ def forward(cfg: MoECfg, x: torch.Tensor, w_router: torch.Tensor,
             router_bias: Optional[torch.Tensor], w1: torch.Tensor, w3: torch.Tensor,
             w2: torch.Tensor, workspace: Optional[torch.Tensor] = None,
             out: Optional[torch.Tensor] = None, routing: Optional[Routing] = None,
-            stream=None, stage_events: Optional[Sequence[torch.cuda.Event]] = None
-            ) -> torch.Tensor:
-    """moe_forward: the layer's MoE branch out[T,H] (the caller adds the residual).
-    Pass `routing` (see ``Routing``) to also receive the routing outputs."""
+            stream=None, stage_events: Optional[Sequence[torch.cuda.Event]] = None,
+            options: Optional[Options] = None) -> torch.Tensor:
+    """moe_forward (moe_forward_ex with `options`): the layer's MoE branch out[T,H]
+    (the caller adds the residual). Pass `routing` (see ``Routing``) to also receive
+    the routing outputs. With shared experts w1, w3, w2 hold N + n_shared experts;
+    with the GELU expert w3 may be None."""
     dt = _io_dtype(cfg)
     T, H, N, F = cfg.T, cfg.H, cfg.N, cfg.F
+    NS = N + (options.n_shared if options is not None else 0)
+    gelu = options is not None and options.activation == "gelu"
     _check(x, "x", (T, H), dt)
     _check(w_router, "w_router", (H, N), dt)
-    _check(w1, "w1", (N, F, H), dt)
-    _check(w3, "w3", (N, F, H), dt)
-    _check(w2, "w2", (N, H, F), dt)
+    _check(w1, "w1", (NS, F, H), dt)
+    if not (gelu and w3 is None):
+        _check(w3, "w3", (NS, F, H), dt)
+    _check(w2, "w2", (NS, H, F), dt)
     if router_bias is not None:
         _check(router_bias, "router_bias", (N,), torch.float32)
+    if options is not None:
+        options.check(T)
     if workspace is None:
-        workspace = make_workspace(cfg, x.device)
+        workspace = make_workspace(cfg, x.device, options)
     if out is None:
         out = torch.empty((T, H), dtype=dt, device=x.device)
     else:
         _check(out, "out", (T, H), dt)
     r = routing
-    args = [ctypes.byref(cfg), _ptr(x), _ptr(w_router), _ptr(router_bias), _ptr(w1), _ptr(w3),
-            _ptr(w2), _ptr(out),
+    args = [_ptr(x), _ptr(w_router), _ptr(router_bias), _ptr(w1), _ptr(w3), _ptr(w2), _ptr(out),
             _ptr(r.topk_idx) if r else None, _ptr(r.topk_w) if r else None,
             _ptr(r.aux_loss) if r else None, _ptr(r.drop_mask) if r else None,
             _ptr(r.expert_counts) if r else None, _ptr(r.kept_counts) if r else None,
             _ptr(workspace), workspace.numel(), _stream(stream)]
-    if stage_events is None:
-        rc = library().moe_forward(*args)
-    else:
+    handles = None
+    if stage_events is not None:
         if len(stage_events) != MOE_NUM_STAGES + 1:
             raise ValueError(f"stage_events needs {MOE_NUM_STAGES + 1} events")
         handles = (ctypes.c_void_p * len(stage_events))(*[e.cuda_event for e in stage_events])
-        rc = library().moe_forward_timed(*args, handles)
+    if options is not None:
+        rc = library().moe_forward_ex(ctypes.byref(cfg), ctypes.byref(options.to_c()), *args,
+                                      handles)
+    elif handles is None:
+        rc = library().moe_forward(ctypes.byref(cfg), *args)
+    else:
+        rc = library().moe_forward_timed(ctypes.byref(cfg), *args, handles)
     if rc != MOE_OK:
         raise MoEError("moe_forward", rc)
     return out

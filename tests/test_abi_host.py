@@ -137,3 +137,56 @@ def test_binding_checks_shapes_without_a_gpu():
     x = torch.zeros(cfg.T, cfg.H)
     with pytest.raises(ValueError):
         moe.route(cfg, x, torch.zeros(cfg.H, cfg.N))   # CPU tensors are refused
+
+
+def _opts(n_shared=0, activation=moe.MOE_ACT_SWIGLU, valid=None):
+    return moe.MoEOptions(n_shared, activation, valid, None, None)
+
+
+def test_workspace_size_ex_matches_base_and_grows_with_shared_experts():
+    lib = moe.library()
+    for c in configs.NAMED:
+        cfg = moe.cfg_from(c)
+        base = moe.workspace_size(cfg)
+        assert lib.moe_workspace_size_ex(ctypes.byref(cfg), None) == base
+        assert lib.moe_workspace_size_ex(ctypes.byref(cfg), ctypes.byref(_opts())) == base
+        s2 = lib.moe_workspace_size_ex(ctypes.byref(cfg), ctypes.byref(_opts(2)))
+        elem = 2 if c.dtype == "bf16" else 4
+        # two more rows per token in the permuted input, h and the expert outputs
+        assert s2 >= base + 2 * c.T * (2 * c.H + c.F) * elem
+
+
+def test_workspace_size_ex_zero_for_bad_options():
+    lib = moe.library()
+    cfg = moe.cfg_from(configs.TINY_F32)
+    for o in (_opts(-1), _opts(moe.MOE_MAX_SHARED + 1), _opts(0, 2), _opts(0, -1)):
+        assert lib.moe_workspace_size_ex(ctypes.byref(cfg), ctypes.byref(o)) == 0
+    assert lib.moe_workspace_size_ex(ctypes.byref(cfg), ctypes.byref(_opts(8))) > 0
+
+
+def test_ex_calls_reject_bad_options_before_any_cuda_call():
+    lib = moe.library()
+    cfg = moe.cfg_from(configs.BF16_T4096)
+    a = _args(cfg)
+    fwd = lambda o, w3=a["w3"]: lib.moe_forward_ex(
+        ctypes.byref(cfg), ctypes.byref(o), a["x"], a["wr"], a["bias"], a["w1"], w3, a["w2"],
+        a["out"], None, None, None, None, None, None, a["ws"], a["ws_bytes"], None, None)
+    assert fwd(_opts(9)) == moe.MOE_EINVAL
+    assert fwd(_opts(0, 5)) == moe.MOE_EINVAL
+    assert fwd(_opts(0, moe.MOE_ACT_SWIGLU), w3=None) == moe.MOE_EINVAL   # SwiGLU needs W3
+    bad_kl = moe.MoEOptions(0, 0, None, 0x7002, None)
+    assert fwd(bad_kl) == moe.MOE_EALIGN
+    rc = lib.moe_route_ex(ctypes.byref(cfg), ctypes.byref(_opts(-3)), a["x"], a["wr"], None,
+                          0x30000, 0x40000, 0x50000, 0x60000, None, None, a["ws"],
+                          a["ws_bytes"], None)
+    assert rc == moe.MOE_EINVAL
+    # the base workspace is too small once shared experts add rows
+    assert fwd(_opts(1)) == moe.MOE_EWORKSPACE
+
+
+def test_options_binding_checks_without_a_gpu():
+    import torch
+    with pytest.raises(ValueError):
+        moe.Options(activation="relu").to_c()
+    with pytest.raises(ValueError):
+        moe.Options(valid_mask=torch.ones(4, dtype=torch.uint8)).check(4)   # CPU tensor

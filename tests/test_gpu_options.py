@@ -1,0 +1,308 @@
+"""Parity of the layer options (shared experts, the GELU expert, a valid-token mask,
+the KL and variance balance losses) through moe_forward_ex / moe_route_ex with the
+fp64 oracle on the same seeded inputs.
+
+Criteria: those of the base parity tests, taken over the valid tokens, plus
+* padding tokens: topk_idx -1, topk_w 0, every slot dropped, output exactly 0;
+* with shared experts a token whose routed slots were all dropped still gets the
+  shared experts' output, so the exact-zero check of such rows applies only
+  without them;
+* aux_kl within 1e-6 relative of the oracle's value: both sides take the logarithms
+  of the same integer counts in double (when a near tie moved a slot, the reference
+  is the oracle's KL of the GPU's own counts);
+* aux_std2 within 2e-4 relative (plus 1e-12 absolute) of the oracle's value: the GPU
+  sums (P - 1/N)^2 of fp32 probabilities, in fp32 inside a block and in double
+  across blocks, and its probabilities differ from the fp64 ones by the router's
+  accumulation rounding (about 1e-6 relative).
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as orc
+from mixture_experts_layer_102_b300 import configs, inputs, moe
+from mixture_experts_layer_102_b300.configs import MoEConfig
+
+pytestmark = pytest.mark.gpu
+
+TOL = {"bf16": 2e-2, "f32": 1e-4}
+TOL_AUX = 1e-5
+TOL_W = 1e-5
+TOL_KL = 1e-6
+TOL_STD2 = 2e-4
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from mixture_experts_layer_102_b300 import build
+    build.build(quiet=True)
+
+
+def _rel_err(y, r):
+    if r.size == 0:
+        return 0.0
+    rms = np.sqrt(np.mean(r * r))
+    return float(np.max(np.abs(y - r) / (np.abs(r) + rms + 1e-30)))
+
+
+def run_opts(cfg, inp, n_shared=0, activation="swiglu", mask=None):
+    c = moe.cfg_from(cfg)
+    dev = moe.to_device(inp)
+    vm = None if mask is None else torch.from_numpy(mask).cuda()
+    kl = torch.full((1,), -7.0, device="cuda")
+    s2 = torch.full((1,), -7.0, device="cuda")
+    opts = moe.Options(n_shared, activation, vm, kl, s2)
+    ws = moe.make_workspace(c, options=opts)
+    routing = moe.new_routing(c)
+    w3 = None if activation == "gelu" else dev.w3
+    out = moe.forward(c, dev.x, dev.w_router, dev.router_bias, dev.w1, w3, dev.w2,
+                      workspace=ws, routing=routing, options=opts)
+    assert moe.get_status(ws) == 0
+    g = {k: getattr(routing, k).cpu().numpy() for k in
+         ("topk_idx", "topk_w", "aux_loss", "drop_mask", "expert_counts", "kept_counts")}
+    g["out"] = out.float().cpu().numpy()
+    g["aux_kl"] = float(kl.item())
+    g["aux_std2"] = float(s2.item())
+    return g, (c, dev, ws, opts)
+
+
+def oracle_opts(cfg, inp, n_shared=0, activation="swiglu", mask=None, token_sample=None):
+    x, wr = inp.values("x"), inp.values("w_router")
+    return orc.moe_forward(x, wr, inp.router_bias, inp.values("w1"),
+                           None if activation == "gelu" else inp.values("w3"),
+                           inp.values("w2"), cfg.k, cfg.capacity_factor,
+                           token_sample=token_sample, n_shared=n_shared,
+                           activation=activation, valid_mask=mask)
+
+
+def compare_opts(cfg, g, ref, mask, n_shared):
+    T, k, N = cfg.T, cfg.k, cfg.N
+    valid = np.ones(T, bool) if mask is None else mask.astype(bool)
+    pad = ~valid
+    assert (g["topk_idx"][pad] == -1).all() and (g["topk_w"][pad] == 0).all()
+    assert (g["drop_mask"][pad] == 1).all()
+    v = np.nonzero(valid)[0]
+    idx_g = g["topk_idx"].astype(np.int64)
+    idx_r = ref.topk_idx
+    set_ties = set(ref.near_tie_set.tolist())
+    order_ties = set(ref.near_tie_order.tolist())
+    same_set = (np.sort(idx_g, axis=1) == np.sort(idx_r, axis=1)).all(axis=1)
+    flipped = np.nonzero(~same_set)[0]
+    assert set(flipped.tolist()) <= set_ties, f"tokens routed differently: {flipped[:10]}"
+    reordered = np.nonzero(same_set & (idx_g != idx_r).any(axis=1))[0]
+    assert set(reordered.tolist()) <= order_ties, f"slot order differs: {reordered[:10]}"
+    for t in flipped:
+        kth = np.sort(ref.logits[t])[::-1][k - 1]
+        assert (ref.logits[t, idx_g[t]] >= kth - orc.NEAR_TIE_MARGIN).all()
+
+    exact = (idx_g == idx_r).all(axis=1) & valid
+    assert np.abs(g["topk_w"][exact] - ref.topk_w[exact]).max(initial=0.0) <= TOL_W
+    assert abs(float(g["aux_loss"][0]) - ref.aux_loss) <= TOL_AUX, (g["aux_loss"], ref.aux_loss)
+
+    C = ref.capacity
+    counts_g = np.bincount(idx_g[v].ravel(), minlength=N)
+    assert (g["expert_counts"] == counts_g).all()
+    if len(flipped) == 0:
+        assert (g["expert_counts"] == ref.expert_counts).all()
+        assert (g["drop_mask"] == ref.drop_mask).all()
+        assert (g["kept_counts"] == ref.kept_counts).all()
+        kl_ref = ref.aux_kl
+    else:
+        # the GPU's capacity decisions must be the valid ones for its own routing:
+        # each expert keeps its first C slots in token order
+        sel_g, drop_g = idx_g[v], g["drop_mask"][v]
+        for e in range(N):
+            kept = drop_g[sel_g == e] == 0
+            want = np.arange(kept.size) < (C if C is not None else kept.size)
+            assert (kept == want).all()
+        kl_ref = orc.aux_kl_uniform(idx_g[v], N, k)
+    if C is not None:
+        assert (g["kept_counts"] == np.minimum(counts_g, C)).all()
+    else:
+        assert g["drop_mask"][v].sum() == 0
+
+    if math.isinf(kl_ref):
+        assert g["aux_kl"] == math.inf
+    else:
+        assert abs(g["aux_kl"] - kl_ref) <= TOL_KL * max(1.0, abs(kl_ref)), (g["aux_kl"], kl_ref)
+    if math.isnan(ref.aux_std2):
+        assert math.isnan(g["aux_std2"])
+    else:
+        assert abs(g["aux_std2"] - ref.aux_std2) <= TOL_STD2 * abs(ref.aux_std2) + 1e-12, \
+            (g["aux_std2"], ref.aux_std2)
+
+    rows = ref.tokens
+    keep = np.ones(len(rows), dtype=bool)
+    if len(flipped):
+        touched = set()
+        for t in flipped:
+            touched |= set(idx_g[t].tolist()) ^ set(idx_r[t].tolist())
+        keep = np.array([not (set(idx_r[t].tolist()) & touched) for t in rows])
+    assert (g["out"][rows[~valid[rows]]] == 0).all()
+    dropped_all = ref.drop_mask[rows].all(axis=1) & valid[rows]
+    live = keep & valid[rows] & (~dropped_all if n_shared == 0 else True)
+    err = _rel_err(g["out"][rows[live]], ref.out[live])
+    assert err <= TOL[cfg.dtype], f"output relative error {err:.3e} > {TOL[cfg.dtype]}"
+    if n_shared == 0:
+        assert (g["out"][rows[dropped_all & keep]] == 0).all()
+    return dict(err=err, flipped=len(flipped), valid=int(valid.sum()))
+
+
+def check_opts(cfg, n_shared=0, activation="swiglu", seq_len=None, token_sample=None):
+    inp = inputs.make_inputs(cfg, n_shared=n_shared)
+    mask = None if seq_len is None else inputs.make_valid_mask(cfg.T, seq_len, cfg.seed)
+    g, _ = run_opts(cfg, inp, n_shared, activation, mask)
+    ref = oracle_opts(cfg, inp, n_shared, activation, mask, token_sample)
+    return compare_opts(cfg, g, ref, mask, n_shared)
+
+
+# (workload, shared experts, activation, sequence length of the padding mask or None)
+CASES = [
+    (configs.TINY_F32.with_(name="f32_shared2_tight", capacity_factor=0.6), 2, "swiglu", None),
+    (configs.TINY_F32.with_(name="f32_gelu"), 0, "gelu", None),
+    (configs.TINY_F32.with_(name="f32_masked", capacity_factor=1.0), 0, "swiglu", 16),
+    (MoEConfig("f32_masked_shared_gelu", 300, 192, 5, 2, 320, 0.9, "f32", seed=31), 1, "gelu", 50),
+    (MoEConfig("bf16_shared1_ragged", 1000, 256, 8, 2, 384, 1.25, "bf16", seed=21), 1, "swiglu",
+     None),
+    (MoEConfig("bf16_gelu_ragged", 1000, 256, 8, 2, 384, 1.25, "bf16", seed=22), 0, "gelu", None),
+    (MoEConfig("bf16_gelu_edge_h320_f192", 777, 320, 6, 2, 192, 1.1, "bf16", seed=23), 0, "gelu",
+     None),
+    (MoEConfig("bf16_masked_ragged", 1000, 256, 8, 2, 384, 1.0, "bf16", seed=24), 0, "swiglu",
+     128),
+    (MoEConfig("bf16_masked_shared2_gelu", 1500, 256, 16, 2, 256, 1.25, "bf16", seed=25), 2,
+     "gelu", 200),
+    # 256-row tiles on CTA pairs
+    (MoEConfig("bf16_pair_shared1", 3000, 256, 4, 2, 384, 1.25, "bf16", seed=26), 1, "swiglu",
+     None),
+    (MoEConfig("bf16_pair_gelu_masked", 4096, 128, 4, 2, 128, 1.02, "bf16", seed=27,
+               zipf_bias=True), 0, "gelu", 512),
+    (MoEConfig("bf16_zipf_masked_shared8", 2048, 128, 64, 2, 128, 1.2, "bf16", seed=28,
+               zipf_bias=True), 8, "swiglu", 100),
+    # k + n_shared = 40 slots per token
+    (MoEConfig("bf16_k32_shared8", 96, 64, 64, 32, 64, None, "bf16", seed=29), 8, "swiglu", 16),
+    # five tokens per warp in the routing decisions (ranks kept in memory past four)
+    (MoEConfig("bf16_t100000_masked_shared1", 100000, 64, 8, 2, 64, 1.25, "bf16", seed=30), 1,
+     "swiglu", 300),
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=lambda c: c[0].name)
+def test_options_elementwise(case):
+    cfg, n_shared, act, seq_len = case
+    check_opts(cfg, n_shared, act, seq_len)
+
+
+def test_bench_shape_with_every_option_sampled():
+    cfg = configs.BF16_T4096
+    inp = inputs.make_inputs(cfg, n_shared=1)
+    mask = inputs.make_valid_mask(cfg.T, 1024, cfg.seed)
+    g, _ = run_opts(cfg, inp, 1, "gelu", mask)
+    sample = np.random.default_rng(5).choice(cfg.T, size=192, replace=False)
+    ref = oracle_opts(cfg, inp, 1, "gelu", mask, np.sort(sample))
+    compare_opts(cfg, g, ref, mask, 1)
+
+
+@pytest.mark.parametrize("c", [configs.BF16_T4096, configs.FINEGRAINED_T16384],
+                         ids=lambda c: c.name)
+def test_losses_on_named_workloads(c):
+    inp = inputs.make_inputs(c, with_experts=False)
+    dev_x = moe.to_torch(inp.x, c.dtype).cuda()
+    dev_wr = moe.to_torch(inp.w_router, c.dtype).cuda()
+    bias = None if inp.router_bias is None else torch.from_numpy(inp.router_bias).cuda()
+    cc = moe.cfg_from(c)
+    kl = torch.zeros(1, device="cuda")
+    s2 = torch.zeros(1, device="cuda")
+    opts = moe.Options(aux_kl=kl, aux_std2=s2)
+    ws = moe.make_workspace(cc, options=opts)
+    r = moe.route(cc, dev_x, dev_wr, bias, workspace=ws, options=opts)
+    assert moe.get_status(ws) == 0
+    ref = orc.route(inp.values("x"), inp.values("w_router"), inp.router_bias, c.k,
+                    c.capacity_factor)
+    idx_g = r.topk_idx.cpu().numpy().astype(np.int64)
+    kl_ref = orc.aux_kl_uniform(idx_g, c.N, c.k)   # of the GPU's own counts
+    assert abs(kl.item() - kl_ref) <= TOL_KL * max(1.0, abs(kl_ref))
+    assert abs(s2.item() - ref["aux_std2"]) <= TOL_STD2 * abs(ref["aux_std2"]) + 1e-12
+    assert abs(r.aux_loss.item() - ref["aux_loss"]) <= TOL_AUX
+
+
+def test_all_padding_gives_zeros():
+    cfg = MoEConfig("bf16_all_padding", 500, 128, 8, 2, 128, 1.25, "bf16", seed=32)
+    inp = inputs.make_inputs(cfg, n_shared=1)
+    mask = np.zeros(cfg.T, np.uint8)
+    g, _ = run_opts(cfg, inp, 1, "swiglu", mask)
+    assert (g["out"] == 0).all() and (g["topk_idx"] == -1).all() and (g["drop_mask"] == 1).all()
+    assert float(g["aux_loss"][0]) == 0.0 and g["aux_kl"] == 0.0 and g["aux_std2"] == 0.0
+    assert g["expert_counts"].sum() == 0 and g["kept_counts"].sum() == 0
+
+
+def test_single_valid_token_single_expert_variance_is_nan():
+    # T_valid * N = 1: the unbiased variance of one probability is undefined
+    cfg = MoEConfig("f32_one_valid", 4, 64, 1, 1, 64, None, "f32", seed=33)
+    inp = inputs.make_inputs(cfg)
+    mask = np.array([0, 0, 1, 0], np.uint8)
+    g, _ = run_opts(cfg, inp, 0, "swiglu", mask)
+    ref = oracle_opts(cfg, inp, 0, "swiglu", mask)
+    assert math.isnan(ref.aux_std2) and math.isnan(g["aux_std2"])
+    compare_opts(cfg, g, ref, mask, 0)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_base_options_are_bit_identical_to_the_base_call(dtype):
+    cfg = MoEConfig(f"{dtype}_base_vs_ex", 1200, 128, 8, 2, 192, 1.1, dtype, seed=34)
+    inp = inputs.make_inputs(cfg)
+    dev = moe.to_device(inp)
+    c = moe.cfg_from(cfg)
+    base = moe.forward(c, dev.x, dev.w_router, dev.router_bias, dev.w1, dev.w3, dev.w2)
+    r_base = moe.new_routing(c)
+    moe.forward(c, dev.x, dev.w_router, dev.router_bias, dev.w1, dev.w3, dev.w2, routing=r_base)
+    # default options, and an all-valid mask, go through the *_ex path
+    for mask in (None, torch.ones(cfg.T, dtype=torch.uint8, device="cuda")):
+        r = moe.new_routing(c)
+        ex = moe.forward(c, dev.x, dev.w_router, dev.router_bias, dev.w1, dev.w3, dev.w2,
+                         routing=r, options=moe.Options(valid_mask=mask))
+        assert torch.equal(ex, base)
+        for name in ("topk_idx", "topk_w", "aux_loss", "drop_mask", "expert_counts",
+                     "kept_counts"):
+            assert torch.equal(getattr(r, name), getattr(r_base, name)), name
+
+
+def test_route_ex_matches_forward_ex():
+    cfg = MoEConfig("bf16_route_ex", 1500, 256, 16, 2, 256, 1.0, "bf16", seed=35)
+    inp = inputs.make_inputs(cfg, n_shared=2)
+    mask = inputs.make_valid_mask(cfg.T, 100, cfg.seed)
+    g, (c, dev, ws, opts) = run_opts(cfg, inp, 2, "swiglu", mask)
+    kl2 = torch.zeros(1, device="cuda")
+    s22 = torch.zeros(1, device="cuda")
+    ropts = moe.Options(2, "swiglu", opts.valid_mask, kl2, s22)
+    r = moe.route(c, dev.x, dev.w_router, dev.router_bias, workspace=ws, options=ropts)
+    assert moe.get_status(ws) == 0
+    for name in ("topk_idx", "topk_w", "aux_loss", "drop_mask", "expert_counts", "kept_counts"):
+        assert (getattr(r, name).cpu().numpy() == g[name]).all(), name
+    assert kl2.item() == g["aux_kl"] and s22.item() == g["aux_std2"]
+
+
+def test_repeat_calls_with_options_are_bit_identical():
+    cfg = MoEConfig("bf16_repeat_opts", 2000, 256, 8, 2, 256, 1.25, "bf16", seed=36)
+    inp = inputs.make_inputs(cfg, n_shared=1)
+    mask = inputs.make_valid_mask(cfg.T, 256, cfg.seed)
+    g1, (c, dev, ws, opts) = run_opts(cfg, inp, 1, "gelu", mask)
+    out2 = moe.forward(c, dev.x, dev.w_router, dev.router_bias, dev.w1, None, dev.w2,
+                       workspace=ws, options=opts)
+    assert moe.get_status(ws) == 0
+    assert (out2.float().cpu().numpy() == g1["out"]).all()
+
+
+def test_bad_options_are_refused():
+    cfg = configs.TINY_F32
+    inp = inputs.make_inputs(cfg)
+    dev = moe.to_device(inp)
+    c = moe.cfg_from(cfg)
+    with pytest.raises(moe.MoEError):   # the library refuses the option itself
+        moe.make_workspace(c, options=moe.Options(n_shared=moe.MOE_MAX_SHARED + 1))
+    with pytest.raises(ValueError):
+        moe.forward(c, dev.x, dev.w_router, None, dev.w1, dev.w3, dev.w2,
+                    options=moe.Options(n_shared=1))   # weights hold only N experts
