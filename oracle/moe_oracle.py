@@ -46,6 +46,19 @@ Options beyond the base layer (the pages' further variants):
   batch at all -- everything (counts, capacity with T_valid, ranks, aux losses) is the
   layer on the valid tokens alone; padding tokens get no expert (index -1, weight 0,
   dropped) and output 0.
+* overflow rerouting instead of dropping (cf-1.com/news/5914943 section 2.3 note
+  moves overflow tokens to other, idle experts; hotelren.com/news/5904824 section 3.4
+  and 2kiu.com/news/2885792 section 2.2 send them to the next-best expert; the
+  capacity-aware routing of hotelren.com/news/3071227 section 4.2 masks the
+  overloaded experts' logits and takes the best remaining one). Reading: one round.
+  After the capacity step, the experts a token may move to are those that still
+  have room (count < C) and that the token did not select; its dropped slots, in
+  slot order, propose the best, second best, ... of them by logit (ties to the lower
+  id), so a token still visits an expert at most once. Each expert accepts the
+  proposals in token order (t, then slot) up to its remaining room C - count; the
+  other slots stay dropped. A rerouted slot keeps its gate weight; its topk_idx
+  becomes the new expert. Counts before capacity and the losses are those of the
+  original routing.
 * two more balance losses: KL(uniform || f) with f_e = counts_e / (T*k)
   (hotelren.com/news/3071227 section 4.2 takes the KL divergence of the expert load
   to the uniform target; its load is normalised by the mask size, here by T*k so that
@@ -172,6 +185,65 @@ def capacity_assign(idx: np.ndarray, N: int, C: Optional[int]):
     return rank, drop, kept
 
 
+def _reroute_candidates(logits_t, idx_t, has_room):
+    """Experts token t may move to, best first: room left, not selected by t; by
+    logit descending, ties to the lower id."""
+    allowed = has_room.copy()
+    allowed[idx_t] = False
+    cand = np.nonzero(allowed)[0]
+    return cand[np.lexsort((cand, -logits_t[cand]))]
+
+
+def reroute_overflow(logits: np.ndarray, idx: np.ndarray, drop: np.ndarray,
+                     counts: np.ndarray, C: Optional[int]):
+    """One round of capacity-aware rerouting of the dropped slots (the reading in the
+    header). Returns (idx_final[T,k], drop_final[T,k], rerouted[T,k] uint8,
+    accepted[N] rerouted slots taken by each expert)."""
+    T, k = idx.shape
+    N = logits.shape[1]
+    idx_f = idx.copy()
+    drop_f = drop.copy()
+    rerouted = np.zeros((T, k), dtype=np.uint8)
+    accepted = np.zeros(N, dtype=np.int64)
+    if C is None:
+        return idx_f, drop_f, rerouted, accepted
+    room = np.maximum(C - counts, 0)
+    has_room = counts < C
+    for t in range(T):
+        dropped = [s for s in range(k) if drop[t, s]]
+        if not dropped:
+            continue
+        cand = _reroute_candidates(logits[t], idx[t], has_room)
+        for j, s in enumerate(dropped):
+            if j >= cand.size:
+                break
+            c = int(cand[j])
+            if accepted[c] < room[c]:
+                accepted[c] += 1
+                idx_f[t, s] = c
+                drop_f[t, s] = 0
+                rerouted[t, s] = 1
+    return idx_f, drop_f, rerouted, accepted
+
+
+def reroute_near_ties(logits: np.ndarray, idx: np.ndarray, drop: np.ndarray,
+                      counts: np.ndarray, C: Optional[int],
+                      margin: float = NEAR_TIE_MARGIN) -> np.ndarray:
+    """Tokens whose m dropped slots' proposals may flip: two of the m+1 best
+    candidates have logits within ``margin``."""
+    out = []
+    if C is None:
+        return np.zeros(0, dtype=np.int64)
+    has_room = counts < C
+    for t in np.nonzero(drop.any(axis=1))[0]:
+        m = int(drop[t].sum())
+        cand = _reroute_candidates(logits[t], idx[t], has_room)
+        v = logits[t][cand[:m + 1]]
+        if v.size >= 2 and (v[:-1] - v[1:] < margin).any():
+            out.append(t)
+    return np.asarray(out, dtype=np.int64)
+
+
 def silu(z: np.ndarray) -> np.ndarray:
     """silu(z) = z * sigmoid(z) = z / (1 + exp(-z))."""
     with np.errstate(over="ignore"):
@@ -247,14 +319,17 @@ class OracleResult:
     near_tie_order: np.ndarray
     aux_kl: float = 0.0
     aux_std2: float = 0.0
+    rerouted: Optional[np.ndarray] = None    # [T,k] uint8, 1 = slot moved by rerouting
+    reroute_ties: Optional[np.ndarray] = None
 
 
-def route(x, w_router, bias, k: int, capacity_factor, valid_mask=None):
+def route(x, w_router, bias, k: int, capacity_factor, valid_mask=None, reroute=False):
     """Steps 1-5 for every token. With ``valid_mask``, the valid tokens are routed as
-    a batch of their own and the padding tokens get index -1, weight 0, dropped."""
+    a batch of their own and the padding tokens get index -1, weight 0, dropped. With
+    ``reroute``, dropped slots take one round of rerouting (``reroute_overflow``)."""
     if valid_mask is not None:
         return _route_masked(x, w_router, bias, k, capacity_factor,
-                             np.asarray(valid_mask).astype(bool))
+                             np.asarray(valid_mask).astype(bool), reroute)
     T = x.shape[0]
     N = w_router.shape[1]
     logits = router_logits(x, w_router, bias)
@@ -266,16 +341,23 @@ def route(x, w_router, bias, k: int, capacity_factor, valid_mask=None):
     C = capacity(T, k, N, capacity_factor)
     rank, drop, kept = capacity_assign(idx, N, C)
     set_ties, order_ties = near_tie_tokens(logits, k)
-    return dict(logits=logits, probs=probs, topk_idx=idx, topk_w=w, aux_loss=aux,
-                aux_kl=aux_kl_uniform(idx, N, k), aux_std2=aux_prob_variance(probs),
-                expert_counts=counts, capacity=C, rank=rank, drop_mask=drop,
-                kept_counts=kept, near_tie_set=set_ties, near_tie_order=order_ties)
+    r = dict(logits=logits, probs=probs, topk_idx=idx, topk_w=w, aux_loss=aux,
+             aux_kl=aux_kl_uniform(idx, N, k), aux_std2=aux_prob_variance(probs),
+             expert_counts=counts, capacity=C, rank=rank, drop_mask=drop,
+             kept_counts=kept, near_tie_set=set_ties, near_tie_order=order_ties,
+             rerouted=np.zeros((T, k), dtype=np.uint8),
+             reroute_ties=np.zeros(0, dtype=np.int64))
+    if reroute:
+        idx_f, drop_f, rer, acc = reroute_overflow(logits, idx, drop, counts, C)
+        r.update(topk_idx=idx_f, drop_mask=drop_f, rerouted=rer, kept_counts=kept + acc,
+                 reroute_ties=reroute_near_ties(logits, idx, drop, counts, C))
+    return r
 
 
-def _route_masked(x, w_router, bias, k, capacity_factor, valid):
+def _route_masked(x, w_router, bias, k, capacity_factor, valid, reroute=False):
     T = x.shape[0]
     v = np.nonzero(valid)[0]
-    r = route(np.asarray(x)[v], w_router, bias, k, capacity_factor)
+    r = route(np.asarray(x)[v], w_router, bias, k, capacity_factor, reroute=reroute)
     full = dict(r)
     full["logits"] = router_logits(x, w_router, bias)
     full["probs"] = full_softmax(full["logits"])
@@ -287,22 +369,25 @@ def _route_masked(x, w_router, bias, k, capacity_factor, valid):
     rank[v] = r["rank"]
     drop = np.ones((T, k), dtype=np.uint8)
     drop[v] = r["drop_mask"]
-    full.update(topk_idx=idx, topk_w=w, rank=rank, drop_mask=drop,
+    rer = np.zeros((T, k), dtype=np.uint8)
+    rer[v] = r["rerouted"]
+    full.update(topk_idx=idx, topk_w=w, rank=rank, drop_mask=drop, rerouted=rer,
                 near_tie_set=v[r["near_tie_set"]], near_tie_order=v[r["near_tie_order"]],
-                valid_tokens=v)
+                reroute_ties=v[r["reroute_ties"]], valid_tokens=v)
     return full
 
 
 def moe_forward(x, w_router, bias, w1, w3, w2, k: int, capacity_factor,
                 token_sample: Optional[np.ndarray] = None, n_shared: int = 0,
-                activation: str = "swiglu", valid_mask=None) -> OracleResult:
+                activation: str = "swiglu", valid_mask=None,
+                reroute: bool = False) -> OracleResult:
     """The whole layer. Routing and capacity always cover every token (capacity
     depends on token order); the expert FFN and the combine are evaluated for the
     tokens in ``token_sample`` (all tokens when None). w1/w3/w2 hold the N routed
     experts followed by ``n_shared`` shared ones (w3 unused for GELU experts)."""
     T, H = x.shape
     N = w_router.shape[1]
-    r = route(x, w_router, bias, k, capacity_factor, valid_mask)
+    r = route(x, w_router, bias, k, capacity_factor, valid_mask, reroute)
     tokens = np.arange(T) if token_sample is None else np.asarray(token_sample, np.int64)
     out = np.zeros((len(tokens), H), dtype=np.float64)
     idx, w, drop = r["topk_idx"], r["topk_w"], r["drop_mask"]

@@ -8,6 +8,7 @@ import pytest
 import oracle
 import oracle.moe_oracle as om
 import test_oracle_pins as pins
+import test_oracle_pins_options as pins_opt
 
 
 def _plant(monkeypatch, name, fn):
@@ -50,8 +51,8 @@ def test_aux_without_division_by_k_is_caught(monkeypatch):
 def test_aux_after_capacity_is_caught(monkeypatch):
     real_route = om.route
 
-    def route_post_cap(x, w_router, bias, k, cf, valid_mask=None):
-        r = real_route(x, w_router, bias, k, cf, valid_mask)
+    def route_post_cap(x, w_router, bias, k, cf, valid_mask=None, reroute=False):
+        r = real_route(x, w_router, bias, k, cf, valid_mask, reroute)
         T, N = r["logits"].shape
         if T:
             f = r["kept_counts"] / float(T * k)
@@ -102,8 +103,8 @@ def test_capacity_priority_reversed_is_caught(monkeypatch):
 def test_renormalising_after_a_drop_is_caught(monkeypatch):
     real_route = om.route
 
-    def route_renorm(x, w_router, bias, k, cf, valid_mask=None):
-        r = real_route(x, w_router, bias, k, cf, valid_mask)
+    def route_renorm(x, w_router, bias, k, cf, valid_mask=None, reroute=False):
+        r = real_route(x, w_router, bias, k, cf, valid_mask, reroute)
         w = r["topk_w"] * (1 - r["drop_mask"])
         s = w.sum(axis=1, keepdims=True)
         r["topk_w"] = np.where(s > 0, w / np.where(s > 0, s, 1.0), 0.0)
@@ -115,9 +116,36 @@ def test_renormalising_after_a_drop_is_caught(monkeypatch):
 def test_ignoring_drops_in_the_combine_is_caught(monkeypatch):
     real_route = om.route
 
-    def route_no_drop(x, w_router, bias, k, cf, valid_mask=None):
-        r = real_route(x, w_router, bias, k, cf, valid_mask)
+    def route_no_drop(x, w_router, bias, k, cf, valid_mask=None, reroute=False):
+        r = real_route(x, w_router, bias, k, cf, valid_mask, reroute)
         r["drop_mask"] = np.zeros_like(r["drop_mask"])
         return r
     _plant(monkeypatch, "route", route_no_drop)
     _fails(pins.test_dropped_slots_give_zero_and_kept_weights_are_not_renormalised)
+
+
+def test_reroute_ignoring_room_is_caught(monkeypatch):
+    real = om.reroute_overflow
+
+    def no_room_check(logits, idx, drop, counts, C):
+        return real(logits, idx, drop, np.zeros_like(counts), C)
+    _plant(monkeypatch, "reroute_overflow", no_room_check)
+    _fails(pins_opt.test_reroute_hand_example_k1)
+
+
+def test_reroute_allowing_own_experts_is_caught(monkeypatch):
+    def cand_own(logits_t, idx_t, has_room):
+        cand = np.nonzero(has_room)[0]
+        return cand[np.lexsort((cand, -logits_t[cand]))]
+    monkeypatch.setattr(om, "_reroute_candidates", cand_own)
+    _fails(pins_opt.test_reroute_excludes_the_tokens_own_experts)
+
+
+def test_reroute_latest_first_is_caught(monkeypatch):
+    real = om.reroute_overflow
+
+    def reversed_order(logits, idx, drop, counts, C):
+        a, b, c, d = real(logits[::-1].copy(), idx[::-1].copy(), drop[::-1].copy(), counts, C)
+        return a[::-1].copy(), b[::-1].copy(), c[::-1].copy(), d
+    _plant(monkeypatch, "reroute_overflow", reversed_order)
+    _fails(pins_opt.test_reroute_hand_example_k1)

@@ -179,3 +179,96 @@ def test_padding_tokens_get_zero_even_with_shared_experts():
                           valid_mask=mask)
     assert (res.out[mask == 0] == 0).all()
     assert np.abs(res.out[mask == 1]).max() > 0
+
+
+# --------------------------------------------------------- overflow rerouting
+
+def _route_logits(logits, k, cf, **kw):
+    """Route with the logits given directly: identity router over H = N."""
+    logits = np.asarray(logits, np.float64)
+    return orc.route(logits, np.eye(logits.shape[1]), None, k, cf, **kw)
+
+
+def test_reroute_hand_example_k1():
+    # C = ceil(0.75 * 5 * 1 / 4) = 1. Tokens 0, 1, 2, 4 pick expert 0, token 3 expert 3.
+    # Experts 1 and 2 have room: token 1 moves to 2 (its better one), token 2 to 1,
+    # token 4 also wants 1 but it is full by then, so it stays dropped.
+    L = [[3, 2, 1, 0], [3, 0, 2, 1], [3, 1, 0, 2], [0, 1, 2, 3], [3, 2, 1.5, 0]]
+    r = _route_logits(L, 1, 0.75, reroute=True)
+    assert r["capacity"] == 1
+    assert r["topk_idx"][:, 0].tolist() == [0, 2, 1, 3, 0]
+    assert r["drop_mask"][:, 0].tolist() == [0, 0, 0, 0, 1]
+    assert r["rerouted"][:, 0].tolist() == [0, 1, 1, 0, 0]
+    assert r["kept_counts"].tolist() == [1, 1, 1, 1]
+    assert r["expert_counts"].tolist() == [4, 0, 0, 1]      # before capacity, unchanged
+
+
+def test_reroute_excludes_the_tokens_own_experts():
+    # C = ceil(1.0 * 3 * 2 / 5) = 2; expert 0 overflows by one (token 2). Token 2's own
+    # expert 4 has room and the larger logit, but a token visits an expert at most
+    # once: it moves to expert 1.
+    L = [[4, 3, 0, 0, 0], [4, 0, 3, 2, 1], [4, 2.5, 0, 1, 3]]
+    r = _route_logits(L, 2, 1.0, reroute=True)
+    assert r["capacity"] == 2
+    assert r["topk_idx"].tolist() == [[0, 1], [0, 2], [1, 4]]
+    assert r["drop_mask"].sum() == 0 and r["rerouted"].tolist() == [[0, 0], [0, 0], [1, 0]]
+    assert r["kept_counts"].tolist() == [2, 2, 1, 0, 1]
+
+
+def test_reroute_slots_take_candidates_in_slot_order():
+    # C = ceil(1.0 * 2 * 2 / 6) = 1: token 1 loses both slots; they take its best and
+    # second best experts with room (3, then 4).
+    L = [[5, 4, 0, 0, 0, 0], [5, 4, 1, 3, 2, 0]]
+    r = _route_logits(L, 2, 1.0, reroute=True)
+    assert r["topk_idx"].tolist() == [[0, 1], [3, 4]]
+    assert r["drop_mask"].sum() == 0
+
+
+def test_reroute_keeps_gate_weights_and_base_when_nothing_overflows():
+    rng = np.random.default_rng(26)
+    x, wr = rng.standard_normal((200, 16)), rng.standard_normal((16, 8))
+    a = orc.route(x, wr, None, 2, 4.0)
+    b = orc.route(x, wr, None, 2, 4.0, reroute=True)         # C = 200: no drops
+    assert a["drop_mask"].sum() == 0 and (a["topk_idx"] == b["topk_idx"]).all()
+    c = orc.route(x, wr, None, 2, 0.5, reroute=True)
+    d = orc.route(x, wr, None, 2, 0.5)
+    assert (c["topk_w"] == d["topk_w"]).all() and c["aux_loss"] == d["aux_loss"]
+    # k = N: no expert left to move to
+    e = orc.route(x, wr, None, 8, 0.5, reroute=True)
+    f = orc.route(x, wr, None, 8, 0.5)
+    assert (e["topk_idx"] == f["topk_idx"]).all() and (e["drop_mask"] == f["drop_mask"]).all()
+
+
+@pytest.mark.parametrize("cf", [0.3, 0.8, 1.0])
+def test_reroute_invariants(cf):
+    cfg = configs.TINY_F32.with_(T=600, N=16, k=2, capacity_factor=cf, zipf_bias=True)
+    inp = inputs.make_inputs(cfg, with_experts=False)
+    base = orc.route(inp.x, inp.w_router, inp.router_bias, 2, cf)
+    r = orc.route(inp.x, inp.w_router, inp.router_bias, 2, cf, reroute=True)
+    C, N = r["capacity"], 16
+    idx, drop, rer = r["topk_idx"], r["drop_mask"], r["rerouted"]
+    final_counts = np.bincount(idx[drop == 0], minlength=N)
+    assert (final_counts == r["kept_counts"]).all() and (final_counts <= C).all()
+    assert r["drop_mask"].sum() <= base["drop_mask"].sum()
+    assert ((rer == 1) <= (base["drop_mask"] == 1)).all()             # only dropped slots move
+    assert (idx[base["drop_mask"] == 0] == base["topk_idx"][base["drop_mask"] == 0]).all()
+    for t in np.nonzero(rer.any(axis=1))[0]:
+        assert len(set(idx[t].tolist())) == 2                          # still distinct
+        for s in np.nonzero(rer[t])[0]:
+            e = idx[t, s]
+            assert e not in base["topk_idx"][t] and base["expert_counts"][e] < C
+    # a slot that stays dropped was turned away: the expert it proposed (its token's
+    # j-th best expert with room that the token did not select, j = the slot's place
+    # among the token's dropped slots) ends up full; brute force over the experts
+    room_left = C - final_counts
+    logits = base["logits"]
+    for t in np.nonzero(drop.any(axis=1))[0]:
+        lost = [s for s in range(2) if base["drop_mask"][t, s]]
+        allowed = sorted((e for e in range(N) if base["expert_counts"][e] < C
+                          and e not in base["topk_idx"][t]),
+                         key=lambda e: (-logits[t, e], e))
+        for j, s in enumerate(lost):
+            if drop[t, s] and j < len(allowed):
+                assert room_left[allowed[j]] == 0, (t, s, allowed[j])
+            elif not drop[t, s]:
+                assert idx[t, s] == allowed[j]
