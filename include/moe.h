@@ -226,13 +226,26 @@ typedef struct {
    * (2kiu.com/news/2885792 section 5.1 penalises std(router_probs)^2); 0 when
    * T_valid = 0, NaN when T_valid*N = 1. */
   float* aux_std2;
+  /* Nonzero: overflow rerouting instead of dropping. One round after the capacity
+   * step (cf-1.com/news/5914943 section 2.3 note moves overflow tokens to idle
+   * experts; hotelren.com/news/5904824 section 3.4 and 2kiu.com/news/2885792
+   * section 2.2 send them to the next-best expert; hotelren.com/news/3071227
+   * section 4.2 masks the overloaded experts and takes the best remaining one):
+   * an expert has room when fewer than C slots chose it; a token's dropped slots,
+   * in slot order, propose its best, second best, ... experts with room that it did
+   * not select (logit descending, ties to the lower id); each expert accepts
+   * proposals in token order up to C - count; the rest stay dropped. A moved slot
+   * keeps its gate weight, topk_idx reports its new expert, drop_mask its final
+   * state and kept_counts the final rows per expert; expert_counts and the losses
+   * stay those of the original routing. No effect without a capacity limit. */
+  int32_t reroute;
 } moe_options;
 
 /* Workspace bytes for cfg with opts (NULL opts: moe_workspace_size); 0 when cfg
  * or opts is invalid or unsupported. Pure host function. */
 size_t moe_workspace_size_ex(const moe_cfg* cfg, const moe_options* opts);
 
-/* moe_route with options: valid_mask, aux_kl and aux_std2 apply; n_shared and
+/* moe_route with options: valid_mask, aux_kl, aux_std2 and reroute apply; n_shared and
  * activation do not change the routing (they only size the workspace). The
  * workspace must hold moe_workspace_size_ex(cfg, opts) bytes. Returns MOE_EINVAL
  * for an out-of-range n_shared or activation. */

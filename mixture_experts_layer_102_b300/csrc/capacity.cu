@@ -9,6 +9,10 @@
 // tokens into expert queues", devpress.csdn.net MoE page section 4.1), copied with
 // 16-byte vectors, one warp per token.
 //
+// With overflow rerouting, a dropped slot whose proposal its new expert accepted goes
+// to that expert's rows after the expert's own count, and its index entry becomes
+// the new expert.
+//
 // Shared experts (hotelren.com/news/5904824 section 3.3) are slots k..k+S-1 of every
 // valid token: row offsets[N+j] + the token's rank among the valid tokens. A padding
 // token (index -1 from the routing decisions) gets no row and every slot dropped.
@@ -57,8 +61,21 @@ __global__ void __launch_bounds__(256) dispatch_kernel(DispatchArgs a) {
         a.drop[j] = 1;
       } else {
         const long long rank = (long long)a.blk_base[(size_t)blk * a.N + e] + a.slot_rank[j];
-        const bool kept = C < 0 || rank < C;
-        if (kept) row = a.offsets[e] + (int)rank;
+        bool kept = C < 0 || rank < C;
+        if (kept) {
+          row = a.offsets[e] + (int)rank;
+        } else if (a.rr_exp != nullptr) {  // rerouted: after the new expert's own rows
+          const int c = a.rr_exp[j];
+          if (c >= 0 && c < a.N) {
+            const long long r2 = (long long)a.rr_base[(size_t)blk * a.N + c] + a.rr_rank[j];
+            const long long own = a.counts[c];  // < C: the expert had room
+            if (r2 < C - own) {
+              kept = true;
+              row = a.offsets[c] + (int)(own + r2);
+              a.idx[j] = c;
+            }
+          }
+        }
         a.drop[j] = kept ? 0 : 1;
       }
     } else if (a.valid == nullptr || a.valid[t] != 0) {  // shared expert N + (sl - k)

@@ -75,9 +75,37 @@ struct SelectArgs {
 // last) the per-expert scan, offsets, tile tables and aux loss.
 cudaError_t launch_route_select(const SelectArgs& a, int nblk, cudaStream_t stream, bool pdl);
 
+// ---------------------------------------------------------------- overflow rerouting
+struct RerouteArgs {
+  const float* part;            // [ksplit][T][N] partial logits
+  int ksplit;
+  const float* bias;            // [N] or null
+  int T, N, k, S;
+  int tpw;                      // the routing-decision kernel's tokens per warp
+  const int32_t* idx;           // [T*k] routed experts (-1: padding)
+  const int32_t* slot_rank;     // [T*k] rank within the routing-decision block
+  const int32_t* blk_base;      // [nblk][N] per-expert bases of those blocks
+  const int32_t* counts;        // [N] slots per expert before capacity
+  int32_t* kept;                // [N+S] rows per expert: capacity's in, final out
+  const int32_t* cap;           // [1] capacity of the call
+  int32_t* rr_exp;              // [T*k] proposed expert of a dropped slot, -1: none
+  int32_t* rr_rank;             // [T*k] rank of the proposal in its block
+  int32_t* rblk;                // [nblk][N] proposals per block, then exclusive bases
+  unsigned* done;               // completion counter, zero between calls
+  int32_t* offsets;             // [N+S+1]
+  int32_t* tile_expert[2];
+  int32_t* tile_row0[2];
+  int32_t* num_mtiles[2];
+  int32_t* tile_first[2];
+  int32_t* user_kept;           // [N] or null
+};
+// One round of rerouting of the slots that capacity dropped, and the final expert
+// layout (the routing-decision kernel's block geometry).
+cudaError_t launch_reroute(const RerouteArgs& a, int nblk, cudaStream_t stream, bool pdl);
+
 // ---------------------------------------------------------------- dispatch
 struct DispatchArgs {
-  const int32_t* idx;           // [T*k]
+  int32_t* idx;                 // [T*k]; a rerouted slot's entry becomes its new expert
   const int32_t* slot_rank;     // [T*k] rank within its routing-decision block
   const int32_t* blk_base;      // [nblk][N] per-expert base of every such block
   int tokens_per_block;
@@ -92,6 +120,10 @@ struct DispatchArgs {
   int A_cap;                    // rows of the permuted buffer
   const void* x;                // [T,H]
   void* xp;                     // [A_cap,H] (may be null when copy is false)
+  const int32_t* rr_exp;        // [T*k] rerouting proposals, or null without rerouting
+  const int32_t* rr_rank;       // [T*k]
+  const int32_t* rr_base;       // [nblk][N]
+  const int32_t* counts;        // [N] slots per expert before capacity
   uint8_t* drop;                // [T*k]
   int32_t* slot_row;            // [T*(k+S)] permuted row of each slot, -1 when dropped
   int32_t* row_token;           // [A_cap]

@@ -14,10 +14,12 @@ namespace {
 
 constexpr size_t kAlign = 256;
 // The workspace starts with 256 bytes that must be zero before the first call
-// (moe_workspace_init): the status word at offset 0 and the routing-decision kernel's
-// completion counter at offset 4, which that kernel returns to zero itself.
+// (moe_workspace_init): the status word at offset 0 and the completion counters of the
+// routing-decision kernel (offset 4) and of the rerouting kernel (offset 8), which
+// those kernels return to zero themselves.
 constexpr int kStatusBytes = 256;
 constexpr size_t kDoneOffset = 4;
+constexpr size_t kRerouteDoneOffset = 8;  // the rerouting kernel's completion counter
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
@@ -30,6 +32,7 @@ struct Opts {
   const uint8_t* valid = nullptr;     // [T] or null
   float* aux_kl = nullptr;
   float* aux_std2 = nullptr;
+  bool reroute = false;
 };
 
 int read_opts(const moe_options* o, Opts* out) {
@@ -42,6 +45,7 @@ int read_opts(const moe_options* o, Opts* out) {
     r.valid = o->valid_mask;
     r.aux_kl = o->aux_kl;
     r.aux_std2 = o->aux_std2;
+    r.reroute = o->reroute != 0;
   }
   *out = r;
   return MOE_OK;
@@ -51,6 +55,7 @@ struct Plan {
   int T, H, N, k, F, dtype;
   int S;                  // shared experts (experts N..N+S-1 of the weight tensors)
   bool masked;            // a valid-token mask is given
+  bool reroute;           // overflow rerouting (only with a capacity limit)
   float cf;               // capacity factor (<= 0: no limit)
   long long C;            // capacity without a mask, -1: no limit (an upper bound with one)
   int A;                  // T*k routing slots
@@ -63,8 +68,8 @@ struct Plan {
   size_t elem;
   size_t off_wrt, off_part, off_psum, off_blk, off_rank, off_idx, off_w, off_drop, off_counts,
       off_kept, off_offsets, off_tile_e[2], off_tile_r[2], off_tile_f[2], off_nmt, off_aux,
-      off_cap, off_bvalid, off_vrank, off_bd2, off_slot_row, off_row_token, off_xp, off_h,
-      off_ye, total;
+      off_cap, off_bvalid, off_vrank, off_bd2, off_rr_exp, off_rr_rank, off_rblk, off_slot_row,
+      off_row_token, off_xp, off_h, off_ye, total;
 };
 
 int check_cfg(const moe_cfg* c) {
@@ -90,6 +95,7 @@ Plan make_plan(const moe_cfg* c, const Opts& o) {
   p.T = c->T; p.H = c->H; p.N = c->N; p.k = c->k; p.F = c->F; p.dtype = c->dtype;
   p.S = o.S;
   p.masked = o.valid != nullptr;
+  p.reroute = o.reroute && c->capacity_factor > 0.0f;
   p.cf = c->capacity_factor;
   p.C = capacity_of(c);  // with a mask the call's C (from T_valid <= T) is no larger
   p.A = c->T * c->k;
@@ -153,6 +159,9 @@ Plan make_plan(const moe_cfg* c, const Opts& o) {
   p.off_bvalid = take((size_t)p.n_sel_blocks * 4);
   p.off_vrank = take(p.masked && p.S > 0 ? T * 4 : 0);
   p.off_bd2 = take((size_t)p.n_sel_blocks * 4);
+  p.off_rr_exp = take(p.reroute ? A * 4 : 0);
+  p.off_rr_rank = take(p.reroute ? A * 4 : 0);
+  p.off_rblk = take(p.reroute ? (size_t)p.n_sel_blocks * N * 4 : 0);
   p.off_slot_row = take(T * (size_t)(p.k + p.S) * 4);
   p.off_row_token = take(Ac * 4);
   p.off_xp = take(Ac * p.H * p.elem);
@@ -242,6 +251,33 @@ int run_route(const Plan& p, const Opts& op, const void* x, const void* w_router
   sa.user_counts = o.counts;
   sa.user_kept = o.kept;
   MOE_TRY(launch_route_select(sa, p.n_sel_blocks, s, p.pdl));
+  RerouteArgs ra;
+  if (p.reroute) {
+    ra.part = part;
+    ra.ksplit = p.ksplit;
+    ra.bias = bias;
+    ra.T = p.T; ra.N = p.N; ra.k = p.k; ra.S = p.S;
+    ra.tpw = p.sel_tpw;
+    ra.idx = o.idx;
+    ra.slot_rank = sa.slot_rank;
+    ra.blk_base = sa.blk_counts;
+    ra.counts = sa.counts;
+    ra.kept = sa.kept;
+    ra.cap = sa.cap;
+    ra.rr_exp = reinterpret_cast<int32_t*>(ws + p.off_rr_exp);
+    ra.rr_rank = reinterpret_cast<int32_t*>(ws + p.off_rr_rank);
+    ra.rblk = reinterpret_cast<int32_t*>(ws + p.off_rblk);
+    ra.done = reinterpret_cast<unsigned*>(ws + kRerouteDoneOffset);
+    ra.offsets = sa.offsets;
+    for (int tb = 0; tb < 2; ++tb) {
+      ra.tile_expert[tb] = sa.tile_expert[tb];
+      ra.tile_row0[tb] = sa.tile_row0[tb];
+      ra.num_mtiles[tb] = sa.num_mtiles[tb];
+      ra.tile_first[tb] = sa.tile_first[tb];
+    }
+    ra.user_kept = o.kept;
+    MOE_TRY(launch_reroute(ra, p.n_sel_blocks, s, p.pdl));
+  }
   rec(2);
   DispatchArgs da;
   da.idx = o.idx;
@@ -256,6 +292,10 @@ int run_route(const Plan& p, const Opts& op, const void* x, const void* w_router
   da.valid = op.valid;
   da.vrank = sa.vrank;
   da.blk_vbase = sa.blk_valid;
+  da.rr_exp = p.reroute ? ra.rr_exp : nullptr;
+  da.rr_rank = p.reroute ? ra.rr_rank : nullptr;
+  da.rr_base = p.reroute ? ra.rblk : nullptr;
+  da.counts = sa.counts;
   da.A_cap = p.A_cap;
   da.x = x;
   da.xp = ws + p.off_xp;

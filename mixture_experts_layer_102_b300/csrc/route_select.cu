@@ -41,6 +41,7 @@
 #include <math.h>
 
 #include "common.cuh"
+#include "expert_layout.cuh"
 #include "internal.h"
 
 namespace moe {
@@ -111,8 +112,7 @@ __device__ double block_sum(double v, double* s_d) {
 __device__ void finish_routing(const SelectArgs& a, int nblk) {
   __shared__ int32_t ip[1024];
   __shared__ float fq[1024];
-  __shared__ int32_t s_counts[MAX_EXPERTS], s_kept[MAX_EXPERTS], s_off[MAX_EXPERTS + 1],
-      s_tile0[2][MAX_EXPERTS + 1];
+  __shared__ int32_t s_counts[MAX_EXPERTS], s_kept[MAX_EXPERTS];
   __shared__ float s_psum[256];
   __shared__ int32_t s_w[32];
   __shared__ double s_d[32];
@@ -226,49 +226,17 @@ __device__ void finish_routing(const SelectArgs& a, int nblk) {
     }
   }
   __syncthreads();
-  if (tid < 32) {  // warp 0: offsets, tile starts and the losses over the experts
+  if (tid < 32) {  // warp 0: the losses over the routed experts
     const int lane = tid;
-    const int per = (Ntot + 31) / 32;  // experts per lane, <= 9
-    const int e0 = min(Ntot, lane * per), e1 = min(Ntot, e0 + per);
-    int off = 0, t1 = 0, t2 = 0;
     float fp = 0.f;
     double lsum = 0.0;
     int empty = 0;
-    for (int e = e0; e < e1; ++e) {
-      off += s_kept[e];
-      t1 += (s_kept[e] + TILE_ROWS_1 - 1) / TILE_ROWS_1;
-      t2 += (s_kept[e] + TILE_ROWS_2 - 1) / TILE_ROWS_2;
-      if (e < N) {
-        fp = fmaf((float)s_counts[e], s_psum[e], fp);
-        if (a.aux_kl != nullptr) {
-          if (s_counts[e] == 0) empty = 1;
-          else lsum += log((double)N * (double)s_counts[e] / ((double)T_valid * (double)a.k));
-        }
+    for (int e = lane; e < N; e += 32) {
+      fp = fmaf((float)s_counts[e], s_psum[e], fp);
+      if (a.aux_kl != nullptr) {
+        if (s_counts[e] == 0) empty = 1;
+        else lsum += log((double)N * (double)s_counts[e] / ((double)T_valid * (double)a.k));
       }
-    }
-    int xo = off, x1 = t1, x2 = t2;  // inclusive scans over the lanes
-#pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-      const int po = __shfl_up_sync(0xffffffffu, xo, d);
-      const int p1 = __shfl_up_sync(0xffffffffu, x1, d);
-      const int p2 = __shfl_up_sync(0xffffffffu, x2, d);
-      if (lane >= d) {
-        xo += po;
-        x1 += p1;
-        x2 += p2;
-      }
-    }
-    int o = xo - off, a1 = x1 - t1, a2 = x2 - t2;
-    for (int e = e0; e < e1; ++e) {
-      s_off[e] = o;
-      s_tile0[0][e] = a1;
-      s_tile0[1][e] = a2;
-      a.tile_first[0][e] = a1;
-      a.tile_first[1][e] = a2;
-      a.offsets[e] = o;
-      o += s_kept[e];
-      a1 += (s_kept[e] + TILE_ROWS_1 - 1) / TILE_ROWS_1;
-      a2 += (s_kept[e] + TILE_ROWS_2 - 1) / TILE_ROWS_2;
     }
 #pragma unroll
     for (int d = 16; d > 0; d >>= 1) fp += __shfl_xor_sync(0xffffffffu, fp, d);
@@ -276,15 +244,7 @@ __device__ void finish_routing(const SelectArgs& a, int nblk) {
       lsum = warp_sum(lsum);
       empty = __any_sync(0xffffffffu, empty);
     }
-    if (lane == 31) {
-      s_off[Ntot] = xo;
-      s_tile0[0][Ntot] = x1;
-      s_tile0[1][Ntot] = x2;
-      a.offsets[Ntot] = xo;
-      a.tile_first[0][Ntot] = x1;
-      a.tile_first[1][Ntot] = x2;
-      *a.num_mtiles[0] = x1;
-      *a.num_mtiles[1] = x2;
+    if (lane == 0) {
       // aux = N * sum_e (counts_e / (T*k)) * (Psum_e / T), T the valid tokens;
       // counts <= T*k and sum_e Psum_e = T keep every term well inside fp32 range
       const float Tf = (float)T_valid;
@@ -298,22 +258,15 @@ __device__ void finish_routing(const SelectArgs& a, int nblk) {
             T_valid == 0 ? 0.f : (float)(d2 / ((double)T_valid * (double)N - 1.0));
     }
   }
-  __syncthreads();
-#pragma unroll
+  ExpertLayout lay;
+  lay.offsets = a.offsets;
   for (int tb = 0; tb < 2; ++tb) {
-    const int rows = tb == 0 ? TILE_ROWS_1 : TILE_ROWS_2;
-    const int32_t* t0 = s_tile0[tb];
-    const int total = t0[Ntot];
-    for (int i = tid; i < total; i += 1024) {
-      int lo = 0, hi = Ntot - 1;  // last expert with t0[e] <= i
-      while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (t0[mid] <= i) lo = mid; else hi = mid - 1;
-      }
-      a.tile_expert[tb][i] = lo;
-      a.tile_row0[tb][i] = s_off[lo] + (i - t0[lo]) * rows;
-    }
+    lay.tile_first[tb] = a.tile_first[tb];
+    lay.num_mtiles[tb] = a.num_mtiles[tb];
+    lay.tile_expert[tb] = a.tile_expert[tb];
+    lay.tile_row0[tb] = a.tile_row0[tb];
   }
+  layout_experts(s_kept, Ntot, lay);
 }
 
 // OPT: the valid-token mask or the variance loss may be in use (read at run time);

@@ -12,6 +12,12 @@ the order x, router weight, router bias, W1, W3, W2):
   the hottest expert gets exactly +2.0 (a Zipf(1.1) profile scaled to 2.0 max).
 * with ``n_shared`` shared experts the expert tensors hold N + n_shared experts drawn
   from the same streams (the first N are the routed experts' weights unchanged).
+* inputs with separated router logits (``make_separated_inputs``), for checking
+  routing decisions exactly: W_r is the identity on the first N hidden dims and zero
+  elsewhere, x[t, :N] is a seeded permutation of 0, 1/64, ..., (N-1)/64 (exact in
+  bf16), the rest of x as above, and the optional bias is the Zipf profile rounded
+  to multiples of 1/128. Every logit is then an exact multiple of 1/128, so two
+  different logits differ by at least 1/128 and equal ones are equal on every side.
 * a valid-token mask (``make_valid_mask``): the batch is cut into sequences of
   ``seq_len`` tokens; sequence b keeps its first L_b tokens, L_b uniform on
   [0, seq_len], and the rest is padding.
@@ -122,3 +128,22 @@ def make_inputs(cfg: MoEConfig, rank: int = 0, with_experts: bool = True,
     else:
         w1 = w3 = w2 = None
     return MoEInputs(cfg.dtype, x, w_router, bias, w1, w3, w2)
+
+
+def make_separated_inputs(cfg: MoEConfig, n_shared: int = 0) -> MoEInputs:
+    """Inputs whose router logits are exact multiples of 1/128 (see the header)."""
+    if cfg.N > cfg.H or cfg.N > 128:
+        raise ValueError("separated logits need N <= H and N <= 128")
+    base = make_inputs(cfg, n_shared=n_shared)
+    g = np.random.Generator(np.random.PCG64(np.random.SeedSequence([cfg.seed, 3000])))
+    T, H, N = cfg.T, cfg.H, cfg.N
+    x = base.values("x").copy()
+    if T:
+        x[:, :N] = np.argsort(g.random((T, N)), axis=1).astype(np.float32) / np.float32(64.0)
+    w_router = np.zeros((H, N), dtype=np.float32)
+    w_router[:N, :N] = np.eye(N, dtype=np.float32)
+    bias = None
+    if base.router_bias is not None:
+        bias = (np.round(base.router_bias.astype(np.float64) * 128.0) / 128.0).astype(np.float32)
+    return MoEInputs(cfg.dtype, _store(x, cfg.dtype), _store(w_router, cfg.dtype), bias,
+                     base.w1, base.w3, base.w2)

@@ -53,26 +53,28 @@ class MoECfg(ctypes.Structure):
 class MoEOptions(ctypes.Structure):
     _fields_ = [("n_shared", ctypes.c_int32), ("activation", ctypes.c_int32),
                 ("valid_mask", ctypes.c_void_p), ("aux_kl", ctypes.c_void_p),
-                ("aux_std2", ctypes.c_void_p)]
+                ("aux_std2", ctypes.c_void_p), ("reroute", ctypes.c_int32)]
 
 
 @dataclass
 class Options:
     """The layer variants of moe_options: shared experts, the GELU expert, a
-    valid-token mask ([T] uint8 or bool on the device) and the two extra balance
-    losses (pass [1] float32 device tensors to receive them)."""
+    valid-token mask ([T] uint8 or bool on the device), the two extra balance
+    losses (pass [1] float32 device tensors to receive them) and overflow rerouting."""
     n_shared: int = 0
     activation: str = "swiglu"
     valid_mask: Optional[torch.Tensor] = None
     aux_kl: Optional[torch.Tensor] = None
     aux_std2: Optional[torch.Tensor] = None
+    reroute: bool = False
 
     def to_c(self) -> MoEOptions:
         if self.activation not in ("swiglu", "gelu"):
             raise ValueError(f"activation must be 'swiglu' or 'gelu', got {self.activation!r}")
         return MoEOptions(int(self.n_shared),
                           MOE_ACT_GELU if self.activation == "gelu" else MOE_ACT_SWIGLU,
-                          _ptr(self.valid_mask), _ptr(self.aux_kl), _ptr(self.aux_std2))
+                          _ptr(self.valid_mask), _ptr(self.aux_kl), _ptr(self.aux_std2),
+                          1 if self.reroute else 0)
 
     def check(self, T: int):
         if self.valid_mask is not None:

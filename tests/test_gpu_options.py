@@ -49,13 +49,13 @@ def _rel_err(y, r):
     return float(np.max(np.abs(y - r) / (np.abs(r) + rms + 1e-30)))
 
 
-def run_opts(cfg, inp, n_shared=0, activation="swiglu", mask=None):
+def run_opts(cfg, inp, n_shared=0, activation="swiglu", mask=None, reroute=False):
     c = moe.cfg_from(cfg)
     dev = moe.to_device(inp)
     vm = None if mask is None else torch.from_numpy(mask).cuda()
     kl = torch.full((1,), -7.0, device="cuda")
     s2 = torch.full((1,), -7.0, device="cuda")
-    opts = moe.Options(n_shared, activation, vm, kl, s2)
+    opts = moe.Options(n_shared, activation, vm, kl, s2, reroute)
     ws = moe.make_workspace(c, options=opts)
     routing = moe.new_routing(c)
     w3 = None if activation == "gelu" else dev.w3
@@ -70,13 +70,14 @@ def run_opts(cfg, inp, n_shared=0, activation="swiglu", mask=None):
     return g, (c, dev, ws, opts)
 
 
-def oracle_opts(cfg, inp, n_shared=0, activation="swiglu", mask=None, token_sample=None):
+def oracle_opts(cfg, inp, n_shared=0, activation="swiglu", mask=None, token_sample=None,
+                reroute=False):
     x, wr = inp.values("x"), inp.values("w_router")
     return orc.moe_forward(x, wr, inp.router_bias, inp.values("w1"),
                            None if activation == "gelu" else inp.values("w3"),
                            inp.values("w2"), cfg.k, cfg.capacity_factor,
                            token_sample=token_sample, n_shared=n_shared,
-                           activation=activation, valid_mask=mask)
+                           activation=activation, valid_mask=mask, reroute=reroute)
 
 
 def compare_opts(cfg, g, ref, mask, n_shared):
@@ -306,3 +307,96 @@ def test_bad_options_are_refused():
     with pytest.raises(ValueError):
         moe.forward(c, dev.x, dev.w_router, None, dev.w1, dev.w3, dev.w2,
                     options=moe.Options(n_shared=1))   # weights hold only N experts
+
+
+# ------------------------------------------------------------ overflow rerouting
+#
+# Inputs with separated router logits (inputs.make_separated_inputs): every logit is
+# an exact multiple of 1/128 on both sides, so every routing and rerouting decision
+# (including equal logits, broken to the lower id by both) must match exactly.
+
+def compare_reroute(cfg, g, ref, mask, n_shared):
+    T = cfg.T
+    valid = np.ones(T, bool) if mask is None else mask.astype(bool)
+    assert (g["topk_idx"] == ref.topk_idx).all(), "final experts differ"
+    assert (g["drop_mask"] == ref.drop_mask).all(), "final drops differ"
+    assert (g["expert_counts"] == ref.expert_counts).all()
+    assert (g["kept_counts"] == ref.kept_counts).all()
+    if ref.capacity is not None:
+        assert (g["kept_counts"] <= ref.capacity).all()
+    assert np.abs(g["topk_w"] - ref.topk_w).max(initial=0.0) <= TOL_W
+    assert abs(float(g["aux_loss"][0]) - ref.aux_loss) <= TOL_AUX
+    rows = ref.tokens
+    vr = valid[rows]
+    dropped_all = ref.drop_mask[rows].all(axis=1) & vr
+    live = vr & (~dropped_all if n_shared == 0 else True)
+    err = _rel_err(g["out"][rows[live]], ref.out[live])
+    assert err <= TOL[cfg.dtype], f"output relative error {err:.3e} > {TOL[cfg.dtype]}"
+    assert (g["out"][rows[~vr]] == 0).all()
+    if n_shared == 0:
+        assert (g["out"][rows[dropped_all]] == 0).all()
+    return dict(err=err, rerouted=int(ref.rerouted.sum()), dropped=int(ref.drop_mask[valid].sum()))
+
+
+def check_reroute(cfg, n_shared=0, activation="swiglu", seq_len=None, token_sample=None):
+    inp = inputs.make_separated_inputs(cfg, n_shared=n_shared)
+    mask = None if seq_len is None else inputs.make_valid_mask(cfg.T, seq_len, cfg.seed)
+    g, _ = run_opts(cfg, inp, n_shared, activation, mask, reroute=True)
+    ref = oracle_opts(cfg, inp, n_shared, activation, mask, token_sample, reroute=True)
+    info = compare_reroute(cfg, g, ref, mask, n_shared)
+    assert info["rerouted"] > 0   # the case exercises rerouting
+    return info
+
+
+REROUTE_CASES = [
+    (MoEConfig("bf16_reroute_zipf_n64", 2048, 128, 64, 2, 128, 1.2, "bf16", seed=41,
+               zipf_bias=True), 0, "swiglu", None),
+    (MoEConfig("bf16_reroute_k4_n32", 1000, 128, 32, 4, 128, 0.8, "bf16", seed=42,
+               zipf_bias=True), 0, "swiglu", None),
+    (MoEConfig("f32_reroute", 300, 192, 16, 2, 320, 1.0, "f32", seed=43, zipf_bias=True), 0,
+     "swiglu", None),
+    (MoEConfig("bf16_reroute_uniform", 3000, 128, 16, 2, 128, 1.05, "bf16", seed=46), 0,
+     "swiglu", None),
+    (MoEConfig("bf16_reroute_k1", 1500, 256, 16, 1, 256, 0.9, "bf16", seed=47, zipf_bias=True),
+     0, "swiglu", None),
+    # 256-row tiles on CTA pairs
+    (MoEConfig("bf16_reroute_pair", 4096, 128, 4, 2, 128, 1.02, "bf16", seed=44,
+               zipf_bias=True), 0, "swiglu", None),
+    (MoEConfig("bf16_reroute_masked_shared2_gelu", 1500, 256, 16, 2, 256, 1.0, "bf16", seed=48,
+               zipf_bias=True), 2, "gelu", 100),
+]
+
+
+@pytest.mark.parametrize("case", REROUTE_CASES, ids=lambda c: c[0].name)
+def test_reroute_elementwise(case):
+    cfg, n_shared, act, seq_len = case
+    check_reroute(cfg, n_shared, act, seq_len)
+
+
+def test_reroute_many_tokens_per_warp_sampled():
+    # 100 000 tokens: five per routing warp; outputs on a seeded sample of rows
+    cfg = MoEConfig("bf16_reroute_t100000", 100000, 128, 32, 2, 64, 1.1, "bf16", seed=45,
+                    zipf_bias=True)
+    sample = np.sort(np.random.default_rng(7).choice(cfg.T, size=3000, replace=False))
+    check_reroute(cfg, 1, "swiglu", 500, token_sample=sample)
+
+
+def test_reroute_without_capacity_changes_nothing():
+    cfg = MoEConfig("bf16_reroute_nocap", 700, 128, 8, 2, 128, None, "bf16", seed=49)
+    inp = inputs.make_inputs(cfg)
+    g0, _ = run_opts(cfg, inp)
+    g1, _ = run_opts(cfg, inp, reroute=True)
+    for name in ("topk_idx", "topk_w", "drop_mask", "kept_counts", "out"):
+        assert (g0[name] == g1[name]).all(), name
+
+
+def test_route_ex_with_reroute_matches_forward_ex():
+    cfg = MoEConfig("bf16_reroute_route", 1500, 128, 32, 2, 128, 1.0, "bf16", seed=50,
+                    zipf_bias=True)
+    inp = inputs.make_separated_inputs(cfg)
+    g, (c, dev, ws, opts) = run_opts(cfg, inp, reroute=True)
+    r = moe.route(c, dev.x, dev.w_router, dev.router_bias, workspace=ws,
+                  options=moe.Options(reroute=True))
+    assert moe.get_status(ws) == 0
+    for name in ("topk_idx", "topk_w", "aux_loss", "drop_mask", "expert_counts", "kept_counts"):
+        assert (getattr(r, name).cpu().numpy() == g[name]).all(), name
