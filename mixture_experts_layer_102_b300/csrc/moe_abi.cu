@@ -63,7 +63,7 @@ struct Plan {
   int ksplit, chunks_per_split;
   int sel_tpw, n_sel_blocks;
   int max_mtiles[2];      // row tiles of 128 and of 256 rows, upper bounds
-  bool pair;              // expert GEMMs on 256-row tiles (CTA pairs)
+  bool pair1, pair2;      // GEMM1 / GEMM2 on 256-row tiles (CTA pairs), else 128-row
   bool pdl;               // kernels after the first launched as programmatic dependents
   size_t elem;
   size_t off_wrt, off_part, off_psum, off_blk, off_rank, off_idx, off_w, off_drop, off_counts,
@@ -124,10 +124,8 @@ Plan make_plan(const moe_cfg* c, const Opts& o) {
   p.n_sel_blocks = (p.T + SELECT_WARPS * p.sel_tpw - 1) / (SELECT_WARPS * p.sel_tpw);
   p.max_mtiles[0] = (p.A_cap + TILE_ROWS_1 - 1) / TILE_ROWS_1 + p.N + p.S;
   p.max_mtiles[1] = (p.A_cap + TILE_ROWS_2 - 1) / TILE_ROWS_2 + p.N + p.S;
-  // Expert GEMM tile shape from the expected rows per expert: large groups go to
-  // CTA pairs (less shared-memory traffic per SM), small ones to single CTAs (less
-  // padding of each expert's last tile, more tiles to spread over the SMs).
-  p.pair = (long long)p.T * (p.k + p.S) >= 1024ll * (p.N + p.S);
+  // Expert GEMM tile shapes (see choose_tiles); this default holds without a bias.
+  p.pair1 = p.pair2 = (long long)p.T * (p.k + p.S) >= 1024ll * (p.N + p.S);
   p.pdl = p.dtype == MOE_BF16;
 
   size_t cur = kStatusBytes;
@@ -169,6 +167,44 @@ Plan make_plan(const moe_cfg* c, const Opts& o) {
   p.off_ye = take(Ac * p.H * p.elem);
   p.total = cur;
   return p;
+}
+
+// Expected rows one expert GEMM computes, over all experts, with tiles of m rows: a
+// routed expert's slot count taken as Normal(mu, sigma^2), the binomial count of
+// uniform routing (mu = T*k/N, sigma^2 = mu*(1 - 1/N)), limited by the capacity;
+// a shared expert has T rows.
+double expected_rows(const Plan& p, int m) {
+  const double mu = (double)p.T * p.k / p.N;
+  const double sigma = sqrt(mu * (1.0 - 1.0 / p.N));
+  double num = 0.0, den = 0.0;
+  for (int i = -320; i <= 320; ++i) {  // z in [-4, 4] in steps of 1/80
+    const double z = i / 80.0;
+    double c = mu + z * sigma;
+    if (c < 0.0) c = 0.0;
+    if (p.C >= 0 && c > (double)p.C) c = (double)p.C;
+    const double w = exp(-0.5 * z * z);
+    num += w * ceil(c / m) * m;
+    den += w;
+  }
+  const double shared = (double)p.S * ceil((double)p.T / m) * m;
+  return p.N * (num / den) + shared;
+}
+
+// Tile shape of each expert GEMM. CTA pairs (256-row tiles) stage a third fewer
+// bytes per SM for the same MMA work, so their load pipeline hides more latency: on
+// B300 they process computed rows about 1.17x faster than single CTAs (128-row
+// tiles), but every expert's last tile is padded to 256 rows. GEMM2 has few column
+// tiles (H/256), so wave quantisation decides it: pairs only from 1024 expected rows
+// per expert. GEMM1 also takes pairs from 512 expected rows per expert when the pair
+// computes at most 12% more rows than single CTAs under the uniform-routing count
+// model; with a router bias the counts are skewed in ways the host cannot see, so
+// GEMM1 keeps the 1024-row rule there.
+void choose_tiles(Plan& p, bool has_bias) {
+  const long long rows = (long long)p.T * (p.k + p.S), per = 1024ll * (p.N + p.S);
+  p.pair2 = rows >= per;
+  p.pair1 = p.pair2;
+  if (!p.pair1 && !has_bias && (long long)p.T * p.k >= 512ll * p.N)
+    p.pair1 = expected_rows(p, TILE_ROWS_2) <= 1.12 * expected_rows(p, TILE_ROWS_1);
 }
 
 int device_check() {
@@ -325,7 +361,7 @@ int run_experts(const Plan& p, const Opts& op, const void* w1, const void* w3, c
   g.N = p.N + p.S;
   g.epi = op.act == MOE_ACT_GELU ? EPI_GELU : EPI_SWIGLU;
   // float32 layers run on CUDA cores over the 128-row table
-  const int tb = (p.dtype == MOE_BF16 && p.pair) ? 1 : 0;
+  int tb = (p.dtype == MOE_BF16 && p.pair1) ? 1 : 0;
   g.pair = tb == 1;
   g.tile_expert = reinterpret_cast<const int32_t*>(ws + p.off_tile_e[tb]);
   g.tile_row0 = reinterpret_cast<const int32_t*>(ws + p.off_tile_r[tb]);
@@ -337,6 +373,13 @@ int run_experts(const Plan& p, const Opts& op, const void* w1, const void* w3, c
   if (p.dtype == MOE_BF16) MOE_TRY(launch_grouped_gemm_tc(g, s, p.pdl));
   else MOE_TRY(launch_grouped_gemm_simt(g, s));
   rec(4);
+  tb = (p.dtype == MOE_BF16 && p.pair2) ? 1 : 0;
+  g.pair = tb == 1;
+  g.tile_expert = reinterpret_cast<const int32_t*>(ws + p.off_tile_e[tb]);
+  g.tile_row0 = reinterpret_cast<const int32_t*>(ws + p.off_tile_r[tb]);
+  g.num_mtiles = reinterpret_cast<const int32_t*>(ws + p.off_nmt) + tb;
+  g.tile_first = reinterpret_cast<const int32_t*>(ws + p.off_tile_f[tb]);
+  g.max_mtiles = p.max_mtiles[tb];
   g.A = ws + p.off_h;
   g.B0 = w2;
   g.B1 = nullptr;
@@ -402,7 +445,8 @@ int forward_impl(const moe_cfg* cfg, const moe_options* opts, const void* x,
       !aligned(topk_w, 4) || !aligned(aux_loss, 4) || !aligned(expert_counts, 4) ||
       !aligned(kept_counts, 4) || !aligned(op.aux_kl, 4) || !aligned(op.aux_std2, 4))
     return MOE_EALIGN;
-  const Plan p = make_plan(cfg, op);
+  Plan p = make_plan(cfg, op);
+  choose_tiles(p, bias != nullptr);
   rc = check_ws(p, workspace, workspace_bytes);
   if (rc != MOE_OK) return rc;
   rc = device_check();

@@ -181,6 +181,9 @@ CASES = [
      None),
     (MoEConfig("bf16_pair_gelu_masked", 4096, 128, 4, 2, 128, 1.02, "bf16", seed=27,
                zipf_bias=True), 0, "gelu", 512),
+    # GEMM1 (GELU) on CTA pairs, GEMM2 on single CTAs
+    (MoEConfig("bf16_mixed_tiles_gelu", 2048, 256, 8, 2, 384, 1.25, "bf16", seed=37), 0, "gelu",
+     None),
     (MoEConfig("bf16_zipf_masked_shared8", 2048, 128, 64, 2, 128, 1.2, "bf16", seed=28,
                zipf_bias=True), 8, "swiglu", 100),
     # k + n_shared = 40 slots per token

@@ -163,6 +163,8 @@ SMALL = [
     MoEConfig("bf16_pair_ragged_t3000", 3000, 256, 4, 2, 384, 1.25, "bf16", seed=12),
     MoEConfig("bf16_pair_edge_h320_f192", 2100, 320, 2, 1, 192, 1.3, "bf16", seed=13),
     MoEConfig("bf16_pair_drops", 4096, 128, 4, 2, 128, 1.02, "bf16", seed=14, zipf_bias=True),
+    # 512 expected rows per expert, no bias: GEMM1 on CTA pairs, GEMM2 on single CTAs
+    MoEConfig("bf16_mixed_tiles_t2048", 2048, 256, 8, 2, 384, 1.25, "bf16", seed=15),
 ]
 
 
