@@ -43,10 +43,9 @@ DEFAULT_CONFIG = configs.BF16_T4096
 FLUSH_BYTES = 256 << 20
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 STAGES = ["router_logits", "route_select", "dispatch", "gemm1_swiglu", "gemm2", "combine"]
-# launches of this library's kernels per forward (T > 0): one per stage, plus the
-# K-major copy of W_r that precedes the tensor-core router of bf16 layers
+# launches of this library's kernels per forward (T > 0): one per stage
 def launches_per_forward(cfg) -> int:
-    return len(STAGES) + (1 if cfg.dtype == "bf16" else 0)
+    return len(STAGES)
 
 
 def parse_args(argv=None):

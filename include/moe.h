@@ -3,7 +3,7 @@
  * Mixture-of-Experts FFN layer.
  *
  * The layer, as the pages state it:
- *   logits = x @ W_r (+ b)                  router: a small linear layer [hidden, N]
+ *   logits = x W_r^T (+ b)                  router: a small linear layer hidden -> N
  *   idx, w = top-k(logits), softmax over the k selected logits
  *   aux    = N * sum_e f_e * P_e            load-balancing loss
  *   C      = ceil(CF * T * k / N)           per-expert capacity; overflow is dropped
@@ -22,8 +22,9 @@
  *    keeps no state between calls.
  *  - Element type of x, w_router, w1, w3, w2, out: float32 (MOE_F32) or bf16
  *    (MOE_BF16) as cfg->dtype says. router_bias is always float32.
- *  - Shapes: x [T,H]; w_router [H,N]; router_bias [N]; w1, w3 [N,F,H] and
- *    w2 [N,H,F] (nn.Linear [out,in] orientation per expert); out [T,H];
+ *  - Shapes: x [T,H]; w_router [N,H]; router_bias [N]; w1, w3 [N,F,H] and
+ *    w2 [N,H,F]; every weight in nn.Linear [out,in] orientation (the router's
+ *    as the pages' nn.Linear(hidden, num_experts), the experts' per expert); out [T,H];
  *    topk_idx [T,k] int32; topk_w [T,k] float32; drop_mask [T,k] uint8
  *    (1 = slot dropped by capacity); expert_counts, kept_counts [N] int32;
  *    aux_loss [1] float32.

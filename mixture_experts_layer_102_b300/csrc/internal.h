@@ -22,17 +22,17 @@ enum Epilogue : int { EPI_PLAIN = 0, EPI_SWIGLU = 1, EPI_GELU = 2 };
 
 // ---------------------------------------------------------------- router
 // Partial logits part[split][t][e] = sum over this split's hidden columns of
-// x[t,h] * w_router[h,e]. dtype: 0 f32, 1 bf16.
+// x[t,h] * w_router[e,h] (W_r [N,H], nn.Linear orientation). dtype: 0 f32, 1 bf16.
 cudaError_t launch_router_logits(int dtype, const void* x, const void* w_router, float* part,
                                  int T, int H, int N, int ksplit, int chunks_per_split,
                                  cudaStream_t stream);
 
-// bf16 router logits on tcgen05: W_r is first copied K-major into wrt [N_pad, H]
-// (N_pad = router_tc_npad(N)); partials as above with the split from router_tc_split.
+// bf16 router logits on tcgen05, partials as above with the split from
+// router_tc_split; the W_r boxes are router_tc_npad(N) rows (zero past N).
 int router_tc_npad(int N);
 void router_tc_split(int T, int H, int* ksplit, int* kc_per_split);
-cudaError_t launch_router_logits_tc(const void* x, const void* w_router, void* wrt, float* part,
-                                    int T, int H, int N, uint32_t* status, cudaStream_t stream,
+cudaError_t launch_router_logits_tc(const void* x, const void* w_router, float* part, int T,
+                                    int H, int N, uint32_t* status, cudaStream_t stream,
                                     bool pdl);
 
 // ---------------------------------------------------------------- routing decisions

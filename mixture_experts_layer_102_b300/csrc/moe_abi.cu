@@ -66,7 +66,7 @@ struct Plan {
   bool pair1, pair2;      // GEMM1 / GEMM2 on 256-row tiles (CTA pairs), else 128-row
   bool pdl;               // kernels after the first launched as programmatic dependents
   size_t elem;
-  size_t off_wrt, off_part, off_psum, off_blk, off_rank, off_idx, off_w, off_drop, off_counts,
+  size_t off_part, off_psum, off_blk, off_rank, off_idx, off_w, off_drop, off_counts,
       off_kept, off_offsets, off_tile_e[2], off_tile_r[2], off_tile_f[2], off_nmt, off_aux,
       off_cap, off_bvalid, off_vrank, off_bd2, off_rr_exp, off_rr_rank, off_rblk, off_slot_row,
       off_row_token, off_xp, off_h, off_ye, total;
@@ -135,7 +135,6 @@ Plan make_plan(const moe_cfg* c, const Opts& o) {
     return o;
   };
   const size_t T = p.T, N = p.N, A = p.A, Ac = p.A_cap, NS = (size_t)p.N + p.S;
-  p.off_wrt = take(p.dtype == MOE_BF16 ? (size_t)router_tc_npad(p.N) * p.H * 2 : 0);
   p.off_part = take((size_t)p.ksplit * T * N * 4);
   p.off_psum = take((size_t)p.n_sel_blocks * N * 4);
   p.off_blk = take((size_t)p.n_sel_blocks * N * 4);
@@ -246,8 +245,7 @@ int run_route(const Plan& p, const Opts& op, const void* x, const void* w_router
   float* part = reinterpret_cast<float*>(ws + p.off_part);
   rec(0);
   if (p.dtype == MOE_BF16)
-    MOE_TRY(launch_router_logits_tc(x, w_router, ws + p.off_wrt, part, p.T, p.H, p.N, status, s,
-                                    false));
+    MOE_TRY(launch_router_logits_tc(x, w_router, part, p.T, p.H, p.N, status, s, false));
   else
     MOE_TRY(launch_router_logits(p.dtype, x, w_router, part, p.T, p.H, p.N, p.ksplit,
                                  p.chunks_per_split, s));

@@ -4,7 +4,8 @@
 // hotelren.com/news/3071227 section 4.1 TopKRouter; stable tie order from
 // 2kiu.com/news/2885792 section 5.3).
 //
-// router_logits_kernel is a split-K fp32 GEMM [T,H]x[H,N] on CUDA cores: N <= 256
+// router_logits_kernel is a split-K fp32 GEMM x W_r^T ([T,H] by W_r [N,H]) on CUDA
+// cores: N <= 256
 // makes it a thin product that is bound by reading x once, and the split over H keeps
 // 2 blocks per SM busy when T is small (decode). The routing decisions that follow
 // (softmax, top-k, gate weights) are in route_select.cu.
@@ -59,9 +60,9 @@ router_logits_kernel(const TIn* __restrict__ x, const TIn* __restrict__ wr,
       *reinterpret_cast<float4*>(dst) = make_float4(v[0], v[1], v[2], v[3]);
       *reinterpret_cast<float4*>(dst + 4) = make_float4(v[4], v[5], v[6], v[7]);
     }
-    for (int i = tid; i < KC * NP; i += 256) {  // W_r rows k0..k0+31, all experts
-      const int kk = i / NP, e = i - kk * NP;
-      ws[i] = (e < N) ? to_f32(wr[(size_t)(k0 + kk) * N + e]) : 0.f;
+    for (int i = tid; i < KC * NP; i += 256) {  // W_r columns k0..k0+31 of every expert
+      const int e = i / KC, kk = i - e * KC;
+      ws[kk * NP + e] = (e < N) ? to_f32(wr[(size_t)e * H + k0 + kk]) : 0.f;
     }
     __syncthreads();
 #pragma unroll

@@ -1,20 +1,18 @@
-// bf16 router logits on the sm_103a tensor cores: logits = x @ W_r, the "small linear
-// layer [hidden, N]" of the router (cf-1.com/news/5914943 section 2.1;
-// 2kiu.com/news/2885792 section 3.1), as split-K fp32 partials part[split][t][e].
+// bf16 router logits on the sm_103a tensor cores: logits = x W_r^T, the small linear
+// layer of the router (cf-1.com/news/5914943 section 2.1; 2kiu.com/news/2885792
+// section 3.1), as split-K fp32 partials part[split][t][e]. W_r is [N, H], the
+// nn.Linear [out, in] orientation, so both MMA operands are K-major 128-byte-swizzled
+// TMA tiles read straight from the caller's tensors.
 //
 // The product is thin (N <= 256 columns against H-long rows of x), so it is bound by
 // reading x once from HBM; on CUDA cores the fine-grained layer's 64 experts made it
-// compute-bound instead. Here:
-//   router_wt_kernel   W_r [H, N] -> W_rT [N_pad, H] (K-major rows, zero rows up to
-//                      N_pad = N rounded up to 16) in the workspace, so both MMA
-//                      operands are K-major 128-byte-swizzled TMA tiles.
-//   router_tc_kernel   one CTA per (128-token tile, K slice): warp 0 streams x and W_rT
-//                      boxes through a 4-stage TMA ring, one thread of warp 1 issues
-//                      tcgen05.mma.cta_group::1 (M=128, N=N_pad, K=16) into a TMEM
-//                      accumulator, warps 2-5 read it back (one token per thread) and
-//                      store the fp32 partial logits of the real experts.
-// The K slices fill the GPU when T is small (decode); the routing-decision kernel sums
-// the slices in a fixed order. Waits are bounded as in the expert GEMM.
+// compute-bound instead. One CTA per (128-token tile, K slice): warp 0 streams x and
+// W_r boxes through a 4-stage TMA ring (the W_r box is N_pad = N rounded up to 16 rows;
+// TMA fills the rows past N with zeros), one thread of warp 1 issues
+// tcgen05.mma.cta_group::1 (M=128, N=N_pad, K=16) into a TMEM accumulator, warps 2-5
+// read it back (one token per thread) and store the fp32 partial logits of the real
+// experts. The K slices fill the GPU when T is small (decode); the routing-decision
+// kernel sums the slices in a fixed order. Waits are bounded as in the expert GEMM.
 #include "common.cuh"
 #include "internal.h"
 #include "tc_util.cuh"
@@ -29,32 +27,13 @@ constexpr int STAGES = 4;
 constexpr uint32_t A_BYTES = 128 * BK * 2;       // 16 KB: 128 tokens x 64
 constexpr int NUM_THREADS = 192;
 
-__global__ void __launch_bounds__(256)
-router_wt_kernel(const __nv_bfloat16* __restrict__ wr, __nv_bfloat16* __restrict__ wrt, int H,
-                 int N, int n_pad) {
-  __shared__ __nv_bfloat16 tile[32][33];
-  const int h0 = blockIdx.x * 32, n0 = blockIdx.y * 32;
-  const int tx = threadIdx.x, ty = threadIdx.y;
-  pdl_wait();
-  pdl_trigger();
-  for (int j = ty; j < 32; j += 8) {
-    const int h = h0 + j, n = n0 + tx;
-    tile[j][tx] = (h < H && n < N) ? wr[(size_t)h * N + n] : __float2bfloat16(0.f);
-  }
-  __syncthreads();
-  for (int j = ty; j < 32; j += 8) {
-    const int n = n0 + j, h = h0 + tx;
-    if (n < n_pad && h < H) wrt[(size_t)n * H + h] = tile[tx][j];
-  }
-}
-
 struct RouterTcArgs {
   float* part;
   int T, N, n_pad;
   int kc_per_split, kc_total;
   uint32_t idesc;
   uint32_t tmem_cols;
-  uint32_t b_bytes;       // one W_rT box: n_pad rows x 128 bytes
+  uint32_t b_bytes;       // one W_r box: n_pad rows x 128 bytes
   uint32_t stage_bytes;   // A box + B box, rounded up to 1024
   uint32_t* status;
 };
@@ -99,7 +78,7 @@ router_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = static_cast<uint32_t>(misc[0]);
-  pdl_wait();  // W_rT comes from the previous kernel
+  pdl_wait();  // x and W_r may come from the caller's previous kernel on the stream
   pdl_trigger();
 
   if (warp == 0) {
@@ -210,19 +189,14 @@ void router_tc_split(int T, int H, int* ksplit, int* kc_per_split) {
   *ksplit = (kc_total + *kc_per_split - 1) / *kc_per_split;
 }
 
-cudaError_t launch_router_logits_tc(const void* x, const void* w_router, void* wrt, float* part,
-                                    int T, int H, int N, uint32_t* status, cudaStream_t stream,
+cudaError_t launch_router_logits_tc(const void* x, const void* w_router, float* part, int T,
+                                    int H, int N, uint32_t* status, cudaStream_t stream,
                                     bool pdl) {
   if (T == 0) return cudaSuccess;
   const int n_pad = router_tc_npad(N);
-  cudaError_t e = launch_kernel(router_wt_kernel, dim3((H + 31) / 32, (n_pad + 31) / 32),
-                                dim3(32, 8), 0, stream, pdl,
-                                static_cast<const __nv_bfloat16*>(w_router),
-                                static_cast<__nv_bfloat16*>(wrt), H, N, n_pad);
-  if (e != cudaSuccess) return e;
   CUtensorMap mX, mW;
   if (!make_map(&mX, x, 2, (uint64_t)H, 0, (uint64_t)T, 128)) return cudaErrorInvalidValue;
-  if (!make_map(&mW, wrt, 2, (uint64_t)H, 0, (uint64_t)n_pad, (uint32_t)n_pad))
+  if (!make_map(&mW, w_router, 2, (uint64_t)H, 0, (uint64_t)N, (uint32_t)n_pad))
     return cudaErrorInvalidValue;
   RouterTcArgs a;
   a.part = part;
@@ -242,11 +216,11 @@ cudaError_t launch_router_logits_tc(const void* x, const void* w_router, void* w
   a.stage_bytes = (A_BYTES + a.b_bytes + 1023u) & ~1023u;
   a.status = status;
   const size_t smem = 1024 + (size_t)STAGES * a.stage_bytes + 256;
-  e = cudaFuncSetAttribute(router_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)smem);
+  const cudaError_t e = cudaFuncSetAttribute(
+      router_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   return launch_kernel(router_tc_kernel, dim3((T + 127) / 128, ksplit), dim3(NUM_THREADS), smem,
-                       stream, true, mX, mW, a);
+                       stream, pdl, mX, mW, a);
 }
 
 }  // namespace moe

@@ -207,7 +207,7 @@ def route(cfg: MoECfg, x: torch.Tensor, w_router: torch.Tensor,
     capacity drop mask, counts."""
     dt = _io_dtype(cfg)
     _check(x, "x", (cfg.T, cfg.H), dt)
-    _check(w_router, "w_router", (cfg.H, cfg.N), dt)
+    _check(w_router, "w_router", (cfg.N, cfg.H), dt)
     if router_bias is not None:
         _check(router_bias, "router_bias", (cfg.N,), torch.float32)
     if options is not None:
@@ -242,7 +242,7 @@ def forward(cfg: MoECfg, x: torch.Tensor, w_router: torch.Tensor,
     NS = N + (options.n_shared if options is not None else 0)
     gelu = options is not None and options.activation == "gelu"
     _check(x, "x", (T, H), dt)
-    _check(w_router, "w_router", (H, N), dt)
+    _check(w_router, "w_router", (N, H), dt)
     _check(w1, "w1", (NS, F, H), dt)
     if not (gelu and w3 is None):
         _check(w3, "w3", (NS, F, H), dt)
@@ -322,9 +322,18 @@ def to_torch(a, dtype: str) -> torch.Tensor:
     return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32))
 
 
+def router_weight_to_device(w_router_hn, dtype: str, device="cuda") -> torch.Tensor:
+    """A router weight given as W_r [H, N] (logits = x @ W_r) in the library's
+    nn.Linear layout [N, H]."""
+    import numpy as np
+    return to_torch(np.ascontiguousarray(np.asarray(w_router_hn).T), dtype).to(device)
+
+
 def to_device(inp, device="cuda") -> DeviceInputs:
-    """Copy an inputs.MoEInputs to the GPU in the library's layouts."""
+    """Copy an inputs.MoEInputs to the GPU in the library's layouts (the router weight,
+    drawn as W_r [H, N], goes over as [N, H])."""
     def up(a):
         return None if a is None else to_torch(a, inp.dtype).to(device)
     bias = None if inp.router_bias is None else torch.from_numpy(inp.router_bias).to(device)
-    return DeviceInputs(up(inp.x), up(inp.w_router), bias, up(inp.w1), up(inp.w3), up(inp.w2))
+    return DeviceInputs(up(inp.x), router_weight_to_device(inp.w_router, inp.dtype, device),
+                        bias, up(inp.w1), up(inp.w3), up(inp.w2))

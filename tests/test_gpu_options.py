@@ -215,7 +215,7 @@ def test_bench_shape_with_every_option_sampled():
 def test_losses_on_named_workloads(c):
     inp = inputs.make_inputs(c, with_experts=False)
     dev_x = moe.to_torch(inp.x, c.dtype).cuda()
-    dev_wr = moe.to_torch(inp.w_router, c.dtype).cuda()
+    dev_wr = moe.router_weight_to_device(inp.w_router, c.dtype)
     bias = None if inp.router_bias is None else torch.from_numpy(inp.router_bias).cuda()
     cc = moe.cfg_from(c)
     kl = torch.zeros(1, device="cuda")
