@@ -143,7 +143,9 @@ int moe_forward(const moe_cfg* cfg, const void* x, const void* w_router,
  * event MOE_NUM_STAGES after the last stage. Stages: 0 router logits, 1 routing
  * decisions (softmax, top-k, gate weights, aux loss, capacity ranks and offsets),
  * 2 dispatch (permute), 3 expert GEMM1 + SwiGLU, 4 expert GEMM2, 5 gated combine.
- * NULL stage_events behaves as moe_forward.
+ * bf16 layers with T > 3968 compute the router logits inside the routing-decision
+ * kernel, so their stage 0 is empty and stage 1 holds both. NULL stage_events behaves
+ * as moe_forward.
  */
 int moe_forward_timed(const moe_cfg* cfg, const void* x, const void* w_router,
                       const float* router_bias, const void* w1, const void* w3,

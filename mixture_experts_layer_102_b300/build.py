@@ -20,7 +20,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(ROOT, "_build")
 LIB_NAME = "libmoe_b300.so"
 LIB_PATH = os.path.join(HERE, LIB_NAME)
-SOURCES = ["moe_abi.cu", "router.cu", "router_tc.cu", "route_select.cu", "reroute.cu",
+SOURCES = ["moe_abi.cu", "router.cu", "router_tc.cu", "route_select.cu", "route_fused.cu",
+           "reroute.cu",
            "capacity.cu", "combine.cu", "gemm_simt.cu", "gemm_tc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -20,15 +20,22 @@ template <int EPI>
 __global__ void __launch_bounds__(256)
 gemm_simt_kernel(const float* __restrict__ A, const float* __restrict__ B0,
                  const float* __restrict__ B1, float* __restrict__ out, int K, int n_cols,
-                 const int32_t* __restrict__ tile_expert, const int32_t* __restrict__ tile_row0,
+                 int N, const int32_t* __restrict__ tile_first,
                  const int32_t* __restrict__ offsets, const int32_t* __restrict__ num_mtiles) {
   constexpr bool SWIGLU = EPI == EPI_SWIGLU;
   const int mt = blockIdx.x;
   pdl_wait();
   pdl_trigger();
   if (mt >= *num_mtiles) return;
-  const int e = tile_expert[mt];
-  const int r0 = tile_row0[mt];
+  __shared__ int32_t tfirst[MAX_EXPERTS + 1];
+  for (int i = threadIdx.x; i <= N; i += blockDim.x) tfirst[i] = tile_first[i];
+  __syncthreads();
+  int e = 0, hi = N - 1;  // the expert of row tile mt: last e with tfirst[e] <= mt
+  while (e < hi) {
+    const int mid = (e + hi + 1) >> 1;
+    if (tfirst[mid] <= mt) e = mid; else hi = mid - 1;
+  }
+  const int r0 = offsets[e] + (mt - tfirst[e]) * BM;
   const int rend = offsets[e + 1];
   const int n0 = blockIdx.y * BN;
   __shared__ float As[BK][BM + 4];
@@ -101,15 +108,15 @@ cudaError_t launch_grouped_gemm_simt(const GroupedGemmArgs& a, cudaStream_t stre
   float* out = static_cast<float*>(a.out);
   if (a.epi == EPI_SWIGLU)
     gemm_simt_kernel<EPI_SWIGLU><<<grid, 256, 0, stream>>>(
-        A, B0, static_cast<const float*>(a.B1), out, a.K, a.n_cols, a.tile_expert, a.tile_row0,
+        A, B0, static_cast<const float*>(a.B1), out, a.K, a.n_cols, a.N, a.tile_first,
         a.offsets, a.num_mtiles);
   else if (a.epi == EPI_GELU)
     gemm_simt_kernel<EPI_GELU><<<grid, 256, 0, stream>>>(A, B0, nullptr, out, a.K, a.n_cols,
-                                                         a.tile_expert, a.tile_row0, a.offsets,
+                                                         a.N, a.tile_first, a.offsets,
                                                          a.num_mtiles);
   else
     gemm_simt_kernel<EPI_PLAIN><<<grid, 256, 0, stream>>>(A, B0, nullptr, out, a.K, a.n_cols,
-                                                          a.tile_expert, a.tile_row0, a.offsets,
+                                                          a.N, a.tile_first, a.offsets,
                                                           a.num_mtiles);
   return cudaGetLastError();
 }

@@ -85,13 +85,13 @@ __device__ __forceinline__ float gelu_erf(float z) {
   return 0.5f * z * (1.0f + erff(z * 0.70710678118654752f));
 }
 
-// Work item w -> (row tile, column tile). Items are grouped by expert (an expert's
-// tiles x all column tiles, experts in order); inside an expert, bands of GROUP_M row
-// tiles sweep the column tiles with the row tile fastest, so the units in flight share
-// a few A tiles and each weight tile of the expert is streamed about once per band.
-// `tfirst` [N+1] holds each expert's first row tile (shared memory).
-__device__ __forceinline__ void raster(int w, const int32_t* tfirst, int N, int n_tiles, int& mt,
-                                       int& nt) {
+// Work item w -> (expert, row tile, column tile). Items are grouped by expert (an
+// expert's tiles x all column tiles, experts in order); inside an expert, bands of
+// GROUP_M row tiles sweep the column tiles with the row tile fastest, so the units in
+// flight share a few A tiles and each weight tile of the expert is streamed about once
+// per band. `tfirst` [N+1] holds each expert's first row tile (shared memory).
+__device__ __forceinline__ void raster(int w, const int32_t* tfirst, int N, int n_tiles, int& e,
+                                       int& mt, int& nt) {
   int lo = 0, hi = N - 1;  // last expert whose first item is <= w
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
@@ -107,11 +107,10 @@ __device__ __forceinline__ void raster(int w, const int32_t* tfirst, int N, int 
   const int gm = min(GROUP_M, tiles - m_first);
   mt = t0 + m_first + in_band % gm;
   nt = in_band / gm;
+  e = lo;
 }
 
 struct TcArgs {
-  const int32_t* tile_expert;
-  const int32_t* tile_row0;
   const int32_t* offsets;
   const int32_t* num_mtiles;
   const int32_t* tile_first;  // [N+1] first row tile of each expert
@@ -190,8 +189,11 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
   pdl_wait();  // tile tables and the A rows come from earlier kernels
   pdl_trigger();
 
-  __shared__ int32_t tfirst[MAX_EXPERTS + 1];
-  for (int i = threadIdx.x; i <= a.N; i += blockDim.x) tfirst[i] = a.tile_first[i];
+  __shared__ int32_t tfirst[MAX_EXPERTS + 1], roff[MAX_EXPERTS + 1];
+  for (int i = threadIdx.x; i <= a.N; i += blockDim.x) {
+    tfirst[i] = a.tile_first[i];
+    roff[i] = a.offsets[i];
+  }
   __syncthreads();
   const int num_mt = *a.num_mtiles;
   const int total = num_mt * a.n_tiles;
@@ -208,10 +210,9 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
       uint32_t used = 0, last_parity = 0;
       bool ok = true;
       for (int w = unit; w < total && ok; w += num_units) {
-        int mt, nt;
-        raster(w, tfirst, a.N, a.n_tiles, mt, nt);
-        const int e = a.tile_expert[mt];
-        const int row0 = a.tile_row0[mt] + (int)rank * 128;
+        int e, mt, nt;
+        raster(w, tfirst, a.N, a.n_tiles, e, mt, nt);
+        const int row0 = roff[e] + (mt - tfirst[e]) * S::TILE_M + (int)rank * 128;
         const int n0 = nt * a.n_per_tile;
         for (int kc = 0; kc < kchunks; ++kc) {
           if (!mbar_wait(empty_bar + 8 * stage, phase ^ 1u, abort_flag, WAIT_LIMIT_NS)) {
@@ -305,11 +306,10 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int w = unit; w < total; w += num_units) {
-      int mt, nt;
-      raster(w, tfirst, a.N, a.n_tiles, mt, nt);
-      const int e = a.tile_expert[mt];
-      const int r = a.tile_row0[mt] + (int)rank * 128 + row_in_cta;
-      const bool valid = r < a.offsets[e + 1];
+      int e, mt, nt;
+      raster(w, tfirst, a.N, a.n_tiles, e, mt, nt);
+      const int r = roff[e] + (mt - tfirst[e]) * S::TILE_M + (int)rank * 128 + row_in_cta;
+      const bool valid = r < roff[e + 1];
       bool ok = mbar_wait(accf_bar + 8 * acc, acc_phase, abort_flag, WAIT_LIMIT_NS);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) {
@@ -477,8 +477,6 @@ cudaError_t launch_grouped_gemm_tc(const GroupedGemmArgs& a, cudaStream_t stream
   if (!make_map(&mB1, swiglu ? a.B1 : a.B0, 3, (uint64_t)a.K, (uint64_t)a.n_cols, (uint64_t)a.N))
     return cudaErrorInvalidValue;
   TcArgs t;
-  t.tile_expert = a.tile_expert;
-  t.tile_row0 = a.tile_row0;
   t.offsets = a.offsets;
   t.num_mtiles = a.num_mtiles;
   t.tile_first = a.tile_first;

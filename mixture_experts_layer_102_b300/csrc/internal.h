@@ -61,19 +61,24 @@ struct SelectArgs {
   int32_t* counts;              // [N+S] slots per expert before capacity
   int32_t* kept;                // [N+S] after capacity
   int32_t* offsets;             // [N+S+1] first permuted row of each expert
-  // GEMM row-tile tables for 128-row tiles [0] and 256-row tiles [1]: expert and
-  // first permuted row of each tile, and the number of tiles
-  int32_t* tile_expert[2];
-  int32_t* tile_row0[2];
+  // GEMM row tiles of 128 rows [0] and 256 rows [1]: first tile of each expert (and
+  // the total), and the number of tiles
   int32_t* num_mtiles[2];
-  int32_t* tile_first[2];       // [N+S+1] first tile of each expert (and the total)
+  int32_t* tile_first[2];       // [N+S+1]
   float* aux;                   // [1]
   int32_t* user_counts;         // optional copies for the caller
   int32_t* user_kept;
 };
 // Softmax, top-k and gate weights, capacity ranks, and (in the block that finishes
-// last) the per-expert scan, offsets, tile tables and aux loss.
+// last) the per-expert scan, offsets, tile starts and aux loss.
 cudaError_t launch_route_select(const SelectArgs& a, int nblk, cudaStream_t stream, bool pdl);
+
+// bf16 layers: the router GEMM and the routing decisions in one launch, writing what
+// launch_route_select writes with blocks of ROUTE_FUSED_TOKENS tokens (a.part, a.ksplit
+// and a.tpw unused). `logits` [T][N] receives the logits with bias, or is null.
+constexpr int ROUTE_FUSED_TOKENS = 128;
+cudaError_t launch_route_fused(const SelectArgs& a, const void* x, const void* w_router, int H,
+                               float* logits, uint32_t* status, cudaStream_t stream, bool pdl);
 
 // ---------------------------------------------------------------- overflow rerouting
 struct RerouteArgs {
@@ -93,8 +98,6 @@ struct RerouteArgs {
   int32_t* rblk;                // [nblk][N] proposals per block, then exclusive bases
   unsigned* done;               // completion counter, zero between calls
   int32_t* offsets;             // [N+S+1]
-  int32_t* tile_expert[2];
-  int32_t* tile_row0[2];
   int32_t* num_mtiles[2];
   int32_t* tile_first[2];
   int32_t* user_kept;           // [N] or null
@@ -143,11 +146,9 @@ struct GroupedGemmArgs {
   int epi;                      // Epilogue: SwiGLU out = silu(A B0^T) * (A B1^T),
                                 // GELU out = gelu(A B0^T), plain out = A B0^T
   bool pair;                    // 256-row tiles on CTA pairs (else 128-row tiles)
-  const int32_t* tile_expert;   // the table that matches the tile shape
-  const int32_t* tile_row0;
-  const int32_t* offsets;
-  const int32_t* num_mtiles;
-  const int32_t* tile_first;    // [N+1] first tile of each expert in that table (N as above)
+  const int32_t* offsets;       // [N+1] first permuted row of each expert (N as above)
+  const int32_t* num_mtiles;    // row tiles of the tile shape
+  const int32_t* tile_first;    // [N+1] first row tile of each expert in that shape
   int max_mtiles;
   uint32_t* status;
 };

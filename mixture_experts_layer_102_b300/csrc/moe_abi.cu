@@ -56,6 +56,7 @@ struct Plan {
   int S;                  // shared experts (experts N..N+S-1 of the weight tensors)
   bool masked;            // a valid-token mask is given
   bool reroute;           // overflow rerouting (only with a capacity limit)
+  bool fused;             // bf16 router GEMM and routing decisions in one launch
   float cf;               // capacity factor (<= 0: no limit)
   long long C;            // capacity without a mask, -1: no limit (an upper bound with one)
   int A;                  // T*k routing slots
@@ -67,7 +68,7 @@ struct Plan {
   bool pdl;               // kernels after the first launched as programmatic dependents
   size_t elem;
   size_t off_part, off_psum, off_blk, off_rank, off_idx, off_w, off_drop, off_counts,
-      off_kept, off_offsets, off_tile_e[2], off_tile_r[2], off_tile_f[2], off_nmt, off_aux,
+      off_kept, off_offsets, off_tile_f[2], off_nmt, off_aux,
       off_cap, off_bvalid, off_vrank, off_bd2, off_rr_exp, off_rr_rank, off_rblk, off_slot_row,
       off_row_token, off_xp, off_h, off_ye, total;
 };
@@ -113,14 +114,22 @@ Plan make_plan(const moe_cfg* c, const Opts& o) {
   if (ksplit < 1) ksplit = 1;
   p.chunks_per_split = (nchunk + ksplit - 1) / ksplit;
   p.ksplit = (nchunk + p.chunks_per_split - 1) / p.chunks_per_split;
-  if (p.dtype == MOE_BF16) {  // the tensor-core router splits K its own way
-    int kcps = 0;
-    router_tc_split(p.T, p.H, &p.ksplit, &kcps);
-  }
-  // router select: one warp per token at a time; enough 8-warp blocks to fill the GPU
   // routing decisions: one token per warp at a time; about 600 blocks at most, so
   // the last block's scan over the blocks stays short
   p.sel_tpw = p.T / (SELECT_WARPS * 600) > 1 ? p.T / (SELECT_WARPS * 600) : 1;
+  // bf16 router: with at least 32 tiles of 128 tokens, one fused launch (router GEMM
+  // and routing decisions, no split of K: its logits, for rerouting, are one "split";
+  // the rerouting kernel and dispatch use its 128-token blocks, 32 warps x 4 tokens).
+  // Fewer tiles leave too few SMs streaming x, so the tensor-core router splits K over
+  // the GPU and the routing decisions follow in their own launch.
+  p.fused = p.dtype == MOE_BF16 && (p.T + ROUTE_FUSED_TOKENS - 1) / ROUTE_FUSED_TOKENS >= 32;
+  if (p.fused) {
+    p.ksplit = 1;
+    p.sel_tpw = ROUTE_FUSED_TOKENS / SELECT_WARPS;
+  } else if (p.dtype == MOE_BF16) {
+    int kcps = 0;
+    router_tc_split(p.T, p.H, &p.ksplit, &kcps);
+  }
   p.n_sel_blocks = (p.T + SELECT_WARPS * p.sel_tpw - 1) / (SELECT_WARPS * p.sel_tpw);
   p.max_mtiles[0] = (p.A_cap + TILE_ROWS_1 - 1) / TILE_ROWS_1 + p.N + p.S;
   p.max_mtiles[1] = (p.A_cap + TILE_ROWS_2 - 1) / TILE_ROWS_2 + p.N + p.S;
@@ -145,11 +154,7 @@ Plan make_plan(const moe_cfg* c, const Opts& o) {
   p.off_counts = take(NS * 4);
   p.off_kept = take(NS * 4);
   p.off_offsets = take((NS + 1) * 4);
-  for (int tb = 0; tb < 2; ++tb) {
-    p.off_tile_e[tb] = take((size_t)p.max_mtiles[tb] * 4);
-    p.off_tile_r[tb] = take((size_t)p.max_mtiles[tb] * 4);
-    p.off_tile_f[tb] = take((NS + 1) * 4);
-  }
+  for (int tb = 0; tb < 2; ++tb) p.off_tile_f[tb] = take((NS + 1) * 4);
   p.off_nmt = take(8);
   p.off_aux = take(4);
   p.off_cap = take(4);
@@ -243,13 +248,14 @@ int run_route(const Plan& p, const Opts& op, const void* x, const void* w_router
   };
   uint32_t* status = reinterpret_cast<uint32_t*>(ws);
   float* part = reinterpret_cast<float*>(ws + p.off_part);
+  const bool fused = p.fused;
   rec(0);
-  if (p.dtype == MOE_BF16)
+  if (p.dtype == MOE_BF16 && !fused)
     MOE_TRY(launch_router_logits_tc(x, w_router, part, p.T, p.H, p.N, status, s, false));
-  else
+  else if (!fused)
     MOE_TRY(launch_router_logits(p.dtype, x, w_router, part, p.T, p.H, p.N, p.ksplit,
                                  p.chunks_per_split, s));
-  rec(1);
+  rec(1);  // fused: the router runs inside the routing-decision stage
   SelectArgs sa;
   sa.part = part;
   sa.ksplit = p.ksplit;
@@ -276,20 +282,22 @@ int run_route(const Plan& p, const Opts& op, const void* x, const void* w_router
   sa.kept = reinterpret_cast<int32_t*>(ws + p.off_kept);
   sa.offsets = reinterpret_cast<int32_t*>(ws + p.off_offsets);
   for (int tb = 0; tb < 2; ++tb) {
-    sa.tile_expert[tb] = reinterpret_cast<int32_t*>(ws + p.off_tile_e[tb]);
-    sa.tile_row0[tb] = reinterpret_cast<int32_t*>(ws + p.off_tile_r[tb]);
     sa.num_mtiles[tb] = reinterpret_cast<int32_t*>(ws + p.off_nmt) + tb;
     sa.tile_first[tb] = reinterpret_cast<int32_t*>(ws + p.off_tile_f[tb]);
   }
   sa.aux = o.aux;
   sa.user_counts = o.counts;
   sa.user_kept = o.kept;
-  MOE_TRY(launch_route_select(sa, p.n_sel_blocks, s, p.pdl));
+  if (fused)  // the forward's first kernel: not a dependent launch
+    MOE_TRY(launch_route_fused(sa, x, w_router, p.H, p.reroute ? part : nullptr, status, s,
+                               false));
+  else
+    MOE_TRY(launch_route_select(sa, p.n_sel_blocks, s, p.pdl));
   RerouteArgs ra;
   if (p.reroute) {
     ra.part = part;
     ra.ksplit = p.ksplit;
-    ra.bias = bias;
+    ra.bias = fused ? nullptr : bias;  // the fused kernel's logits include the bias
     ra.T = p.T; ra.N = p.N; ra.k = p.k; ra.S = p.S;
     ra.tpw = p.sel_tpw;
     ra.idx = o.idx;
@@ -304,8 +312,6 @@ int run_route(const Plan& p, const Opts& op, const void* x, const void* w_router
     ra.done = reinterpret_cast<unsigned*>(ws + kRerouteDoneOffset);
     ra.offsets = sa.offsets;
     for (int tb = 0; tb < 2; ++tb) {
-      ra.tile_expert[tb] = sa.tile_expert[tb];
-      ra.tile_row0[tb] = sa.tile_row0[tb];
       ra.num_mtiles[tb] = sa.num_mtiles[tb];
       ra.tile_first[tb] = sa.tile_first[tb];
     }
@@ -361,8 +367,6 @@ int run_experts(const Plan& p, const Opts& op, const void* w1, const void* w3, c
   // float32 layers run on CUDA cores over the 128-row table
   int tb = (p.dtype == MOE_BF16 && p.pair1) ? 1 : 0;
   g.pair = tb == 1;
-  g.tile_expert = reinterpret_cast<const int32_t*>(ws + p.off_tile_e[tb]);
-  g.tile_row0 = reinterpret_cast<const int32_t*>(ws + p.off_tile_r[tb]);
   g.offsets = reinterpret_cast<const int32_t*>(ws + p.off_offsets);
   g.num_mtiles = reinterpret_cast<const int32_t*>(ws + p.off_nmt) + tb;
   g.tile_first = reinterpret_cast<const int32_t*>(ws + p.off_tile_f[tb]);
@@ -373,8 +377,6 @@ int run_experts(const Plan& p, const Opts& op, const void* w1, const void* w3, c
   rec(4);
   tb = (p.dtype == MOE_BF16 && p.pair2) ? 1 : 0;
   g.pair = tb == 1;
-  g.tile_expert = reinterpret_cast<const int32_t*>(ws + p.off_tile_e[tb]);
-  g.tile_row0 = reinterpret_cast<const int32_t*>(ws + p.off_tile_r[tb]);
   g.num_mtiles = reinterpret_cast<const int32_t*>(ws + p.off_nmt) + tb;
   g.tile_first = reinterpret_cast<const int32_t*>(ws + p.off_tile_f[tb]);
   g.max_mtiles = p.max_mtiles[tb];

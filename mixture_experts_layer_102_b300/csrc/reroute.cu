@@ -165,8 +165,6 @@ __global__ void __launch_bounds__(1024) reroute_kernel(RerouteArgs a) {
   for (int tb = 0; tb < 2; ++tb) {
     lay.tile_first[tb] = a.tile_first[tb];
     lay.num_mtiles[tb] = a.num_mtiles[tb];
-    lay.tile_expert[tb] = a.tile_expert[tb];
-    lay.tile_row0[tb] = a.tile_row0[tb];
   }
   layout_experts(s_rows, Ntot, lay);
   if (threadIdx.x == 0) *a.done = 0u;  // ready for the next call

@@ -1,0 +1,398 @@
+// Router GEMM and routing decisions of bf16 layers in one launch.
+//
+//   logits = x W_r^T (+ b)      the router's linear layer (cf-1.com/news/5914943 section
+//                               2.1; 2kiu.com/news/2885792 section 3.1)
+//   P = softmax(logits); idx = top-k of the logits, ties to the lower expert id; w =
+//   softmax over the k selected logits (cf-1.com/news/5914943 section 2.1;
+//   hotelren.com/news/3071227 section 4.1; 2kiu.com/news/2885792 section 5.3)
+//   counts, sums of P, capacity ranks in token order, offsets and the aux loss as in
+//   the routing-decision kernel (route_select.cu), whose outputs this kernel writes in
+//   the same form with a block of 128 tokens.
+//
+// One CTA per 128-token tile, 256 threads, no split of K, so the logits never leave
+// the CTA as partial sums:
+//   warp 0      TMA producer: x rows and W_r ([N, H], N_pad = N rounded up to 16 rows,
+//               zero past N) stream through as many 128-byte-swizzled stages as shared
+//               memory holds, so the load pipeline covers HBM latency.
+//   warp 1      TMEM allocator; one thread issues tcgen05.mma.cta_group::1 (M=128,
+//               N=N_pad, K=16) into a TMEM accumulator.
+//   warps 2-5   read the accumulator back (one token per thread: the TMEM lane) and
+//               stage the logits (+ bias) in the freed stage memory; then each thread
+//               makes its token's decisions: softmax by max and sum, the top k by k
+//               passes, each taking the best logit strictly after the previous pick in
+//               the order (logit descending, id ascending), the gate weights, and the
+//               token's row of probabilities.
+//   all warps   per expert, in a fixed order over the tile's rows: the sum of P, the
+//               count, and each slot's rank among the tile's earlier slots of that
+//               expert (its rank in token order inside the tile).
+// The CTA that finishes last (a completion counter, no waiting) runs the same finish
+// as the routing-decision kernel: per-block bases, capacity, losses, expert layout.
+#include <math.h>
+
+#include "common.cuh"
+#include "internal.h"
+#include "route_finish.cuh"
+#include "tc_util.cuh"
+
+namespace moe {
+namespace {
+
+using namespace tc;
+using namespace route;
+
+constexpr int BK = 64;                          // 64 bf16 = one 128-byte swizzle row
+constexpr int TOK = 128;                        // tokens per CTA (TMEM lanes)
+constexpr uint32_t A_BYTES = TOK * BK * 2;      // 16 KB
+constexpr int NUM_THREADS = 256;
+constexpr int MAX_STAGES = 16;
+constexpr int SMEM_OPTIN = 232448;              // bytes of shared memory per block
+
+struct FusedArgs {
+  SelectArgs s;        // outputs, options and workspace arrays of the routing decisions
+  float* logits;       // [T][N] logits with bias, for the rerouting kernel, or null
+  int kc_total;        // H / 64
+  int n_pad, stages;
+  uint32_t idesc, tmem_cols, b_bytes, stage_bytes, region_bytes;
+  uint32_t* status;
+};
+
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+route_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
+                   FusedArgs f) {
+  const SelectArgs& a = f.s;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* base_ptr = smem_raw + (base - raw);
+  const int STAGES = f.stages;
+  const uint32_t full_bar = base + f.region_bytes;
+  const uint32_t empty_bar = full_bar + 8 * MAX_STAGES;
+  const uint32_t accf_bar = empty_bar + 8 * MAX_STAGES;
+  int* misc = reinterpret_cast<int*>(base_ptr + f.region_bytes + 8 * (2 * MAX_STAGES + 1));
+  volatile int* abort_flag = misc + 1;
+  __shared__ float s_bias[256];
+  __shared__ uint8_t s_valid[TOK];
+  __shared__ int is_last;
+  __shared__ double s_dd[32];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int N = a.N, k = a.k;
+  const int m0 = blockIdx.x * TOK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full_bar + 8 * s, 1);
+      mbar_init(empty_bar + 8 * s, 1);
+    }
+    mbar_init(accf_bar, 1);
+    misc[1] = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    prefetch_map(&tmX);
+    prefetch_map(&tmW);
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(misc)),
+                 "r"(f.tmem_cols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  // the bias is the caller's input, not a predecessor's output: read before the wait
+  for (int i = threadIdx.x; i < N; i += NUM_THREADS)
+    s_bias[i] = a.bias != nullptr ? a.bias[i] : 0.f;
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = static_cast<uint32_t>(misc[0]);
+  pdl_wait();  // x and W_r may come from the caller's previous kernel on the stream
+  pdl_trigger();
+
+  if (warp == 0) {
+    if (lane == 0) {  // ---------------------------------------------- TMA producer
+      int stage = 0;
+      uint32_t phase = 0, used = 0, last_parity = 0;
+      bool ok = true;
+      for (int kc = 0; kc < f.kc_total; ++kc) {
+        if (!mbar_wait(empty_bar + 8 * stage, phase ^ 1u, abort_flag, WAIT_LIMIT_NS)) {
+          ok = false;
+          break;
+        }
+        const uint32_t sA = base + stage * f.stage_bytes;
+        const uint32_t fb = full_bar + 8 * stage;
+        mbar_expect_tx(fb, A_BYTES + f.b_bytes);
+        tma_load_2d<1>(sA, &tmX, fb, kc * BK, m0);
+        tma_load_2d<1>(sA + A_BYTES, &tmW, fb, kc * BK, 0);
+        used |= 1u << stage;
+        last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (!ok) {
+        report(f.status, STATUS_WAIT_TIMEOUT);
+        *abort_flag = 1;
+      }
+      for (int s = 0; s < STAGES; ++s)
+        if ((used >> s) & 1u)
+          mbar_wait(full_bar + 8 * s, (last_parity >> s) & 1u, nullptr, DRAIN_LIMIT_NS);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {  // ---------------------------------------------- MMA issuer
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int kc = 0; kc < f.kc_total; ++kc) {
+        if (!mbar_wait(full_bar + 8 * stage, phase, abort_flag, WAIT_LIMIT_NS)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t sA = base + stage * f.stage_bytes;
+        const uint64_t da = sw128_desc(sA);
+        const uint64_t db = sw128_desc(sA + A_BYTES);
+#pragma unroll
+        for (int kk = 0; kk < BK / 16; ++kk)
+          tc_mma<1>(tmem, da + 2 * kk, db + 2 * kk, f.idesc, (kc > 0 || kk > 0) ? 1u : 0u);
+        tc_commit<1>(empty_bar + 8 * stage);
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (!ok) {
+        report(f.status, STATUS_WAIT_TIMEOUT);
+        *abort_flag = 1;
+      }
+      tc_commit<1>(accf_bar);  // also drains: every MMA above is complete when it flips
+    }
+  }
+  // Epilogue shared memory, in the stage region (every load has landed and every MMA
+  // has read its operands once the accumulator barrier flips):
+  //   L  [TOK][N+1] logits, then probabilities     (fp32)
+  //   SEL[TOK][k]   the selected experts            (int32)
+  //   CH [TOK][N]   slot + 1 of a selected expert   (bytes, 0 = not selected)
+  const int LS = N + 1;
+  float* L = reinterpret_cast<float*>(base_ptr);
+  int32_t* SEL = reinterpret_cast<int32_t*>(base_ptr + (size_t)TOK * LS * 4);
+  uint8_t* CH = base_ptr + (size_t)TOK * LS * 4 + (size_t)TOK * k * 4;
+  bool acc_ok = true;
+  if (warp >= 2 && warp < 6) {  // ------------------------------- accumulator -> smem
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;
+    const int t = m0 + r;
+    bool ok = mbar_wait(accf_bar, 0, abort_flag, WAIT_LIMIT_NS);
+    ok = __all_sync(0xffffffffu, ok);
+    if (ok) {
+      tc_fence_after();
+      const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16);
+      for (int c = 0; c < f.n_pad; c += 16) {
+        uint32_t v[16];
+        tmem_ld16(taddr + c, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+          const int e = c + q;
+          if (e < N) {
+            const float l = __uint_as_float(v[q]) + s_bias[e];
+            L[r * LS + e] = l;
+            if (f.logits != nullptr && t < a.T) f.logits[(size_t)t * N + e] = l;
+          }
+        }
+      }
+    } else {
+      if (lane == 0) {
+        report(f.status, STATUS_WAIT_TIMEOUT);
+        *abort_flag = 1;
+      }
+    }
+    acc_ok = ok;
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {  // the accumulator has been read
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(f.tmem_cols)
+                 : "memory");
+  }
+  // ---------------------------------------------------- per-token decisions (4 warps)
+  const bool masked = a.valid != nullptr;
+  const bool want_d2 = a.aux_std2 != nullptr;
+  float d2 = 0.f;
+  if (warp >= 2 && warp < 6) {
+    const int r = (warp & 3) * 32 + lane;
+    const int t = m0 + r;
+    float* row = L + r * LS;
+    uint8_t* ch = CH + (size_t)r * N;
+    for (int e = 0; e < N; ++e) ch[e] = 0;
+    const bool live = acc_ok && t < a.T && (!masked || a.valid[t] != 0);
+    s_valid[r] = live ? 1 : 0;
+    if (live) {
+      float m = -INFINITY;
+      for (int e = 0; e < N; ++e) m = fmaxf(m, row[e]);
+      float sum = 0.f;
+      for (int e = 0; e < N; ++e) sum += expf(row[e] - m);
+      const float inv = 1.f / sum;
+      // top k: pick j is the best logit strictly after pick j-1 in (logit desc, id asc)
+      float pl = INFINITY, l0 = 0.f, zs = 0.f;
+      int pi = -1;
+      for (int j = 0; j < k; ++j) {
+        float bv = -INFINITY;
+        int bi = -1;
+        for (int e = 0; e < N; ++e) {
+          const float v = row[e];
+          const bool after = v < pl || (v == pl && e > pi);
+          if (after && (bi < 0 || v > bv)) {
+            bv = v;
+            bi = e;
+          }
+        }
+        if (bi < 0) {  // only NaN logits leave no candidate: keep the index in range
+          bi = j;
+          bv = row[j];
+        }
+        SEL[r * k + j] = bi;
+        if (j == 0) l0 = bv;
+        zs += expf(bv - l0);
+        pl = bv;
+        pi = bi;
+      }
+      for (int j = 0; j < k; ++j) {  // gate weights: softmax over the k selected logits
+        const int e = SEL[r * k + j];
+        a.idx[(size_t)t * k + j] = e;
+        a.w[(size_t)t * k + j] = expf(row[e] - l0) / zs;
+        ch[e] = (uint8_t)(j + 1);
+      }
+      const float invN = 1.f / (float)N;
+      for (int e = 0; e < N; ++e) {  // the token's probabilities replace its logits
+        const float pe = expf(row[e] - m) * inv;
+        row[e] = pe;
+        if (want_d2) d2 = fmaf(pe - invN, pe - invN, d2);
+      }
+    } else {
+      for (int e = 0; e < N; ++e) row[e] = 0.f;
+      if (t < a.T) {  // padding: no expert, weight 0
+        for (int j = 0; j < k; ++j) {
+          a.idx[(size_t)t * k + j] = -1;
+          a.w[(size_t)t * k + j] = 0.f;
+        }
+      }
+    }
+  }
+  __syncthreads();
+  // ------------------------------------------------------ per-expert column pass
+  // Thread (g, e) covers rows [g*R, g*R + R) of expert e: count, sum of P; the groups'
+  // counts are prefixed in order and every slot gets its rank inside the tile.
+  {
+    int np2 = 1;
+    while (np2 < N) np2 <<= 1;
+    int G = NUM_THREADS / np2;
+    if (G > TOK) G = TOK;
+    const int R = TOK / G;
+    const int e = threadIdx.x % np2, g = threadIdx.x / np2;
+    __shared__ int32_t s_gc[NUM_THREADS];
+    __shared__ float s_gp[NUM_THREADS];
+    int cnt = 0;
+    float ps = 0.f;
+    const bool mine = e < N && g < G;
+    if (mine) {
+      for (int r = g * R; r < g * R + R; ++r) {
+        ps += L[r * LS + e];
+        cnt += CH[(size_t)r * N + e] != 0;
+      }
+      s_gc[g * np2 + e] = cnt;
+      s_gp[g * np2 + e] = ps;
+    }
+    __syncthreads();
+    if (mine) {
+      int rank = 0;
+      for (int h = 0; h < g; ++h) rank += s_gc[h * np2 + e];
+      for (int r = g * R; r < g * R + R; ++r) {
+        const int c = CH[(size_t)r * N + e];
+        if (c != 0) a.slot_rank[(size_t)(m0 + r) * k + (c - 1)] = rank++;
+      }
+      if (g == G - 1) {  // this block's totals, summed over the groups in order
+        int tc = 0;
+        float tp = 0.f;
+        for (int h = 0; h < G; ++h) {
+          tc += s_gc[h * np2 + e];
+          tp += s_gp[h * np2 + e];
+        }
+        a.blk_counts[(size_t)blockIdx.x * N + e] = tc;
+        a.blk_psum[(size_t)blockIdx.x * N + e] = tp;
+      }
+    }
+  }
+  if (masked && warp == 0) {  // valid tokens of the tile: ranks and count
+    int run = 0;
+    for (int c = 0; c < TOK; c += 32) {
+      const bool v = s_valid[c + lane] != 0;
+      const uint32_t b = __ballot_sync(0xffffffffu, v);
+      const int t = m0 + c + lane;
+      if (v && a.S > 0) a.vrank[t] = run + __popc(b & ((1u << lane) - 1u));
+      run += __popc(b);
+    }
+    if (lane == 0) a.blk_valid[blockIdx.x] = run;
+  }
+  if (want_d2) {
+    const double dsum = block_sum((double)d2, s_dd);
+    if (threadIdx.x == 0) a.blk_d2[blockIdx.x] = (float)dsum;
+  }
+  // The last CTA to get here finishes the layer-wide statistics.
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) is_last = atomicAdd(a.done, 1u) == gridDim.x - 1;
+  __syncthreads();
+  if (!is_last) return;
+  __threadfence();
+  finish_routing(a, gridDim.x);
+  if (threadIdx.x == 0) *a.done = 0u;  // ready for the next call
+}
+
+}  // namespace
+
+cudaError_t launch_route_fused(const SelectArgs& s, const void* x, const void* w_router, int H,
+                               float* logits, uint32_t* status, cudaStream_t stream, bool pdl) {
+  if (s.T == 0) return cudaSuccess;
+  FusedArgs f;
+  f.s = s;
+  f.logits = logits;
+  f.status = status;
+  f.kc_total = H / BK;
+  f.n_pad = (s.N + 15) / 16 * 16;
+  uint32_t cols = 32;
+  while ((int)cols < f.n_pad) cols <<= 1;
+  f.tmem_cols = cols;
+  f.b_bytes = (uint32_t)f.n_pad * 128;
+  f.stage_bytes = (A_BYTES + f.b_bytes + 1023u) & ~1023u;
+  // kind::f16 descriptor: D fp32, A/B bf16, K-major, N = n_pad, M = 128
+  f.idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(f.n_pad >> 3) << 17) |
+            ((uint32_t)(TOK >> 4) << 24);
+  cudaFuncAttributes attr;
+  cudaError_t e = cudaFuncGetAttributes(&attr, route_fused_kernel);
+  if (e != cudaSuccess) return e;
+  const size_t epi = (size_t)TOK * (s.N + 1) * 4 + (size_t)TOK * s.k * 4 + (size_t)TOK * s.N;
+  const size_t tail = 8 * (2 * MAX_STAGES + 1) + 16;  // barriers, TMEM address, abort flag
+  const size_t avail = (size_t)SMEM_OPTIN - attr.sharedSizeBytes - 1024 - tail;
+  int stages = (int)(avail / f.stage_bytes);
+  if (stages > MAX_STAGES) stages = MAX_STAGES;
+  if (stages > f.kc_total) stages = f.kc_total > 1 ? f.kc_total : 1;
+  if (stages < 1) return cudaErrorInvalidValue;
+  f.stages = stages;
+  size_t region = (size_t)stages * f.stage_bytes;
+  if (region < epi) region = (epi + 1023) / 1024 * 1024;
+  if (region > avail) return cudaErrorInvalidValue;
+  f.region_bytes = (uint32_t)region;
+  const size_t smem = 1024 + region + tail;
+  CUtensorMap mX, mW;
+  if (!make_map(&mX, x, 2, (uint64_t)H, 0, (uint64_t)s.T, TOK)) return cudaErrorInvalidValue;
+  if (!make_map(&mW, w_router, 2, (uint64_t)H, 0, (uint64_t)s.N, (uint32_t)f.n_pad))
+    return cudaErrorInvalidValue;
+  e = cudaFuncSetAttribute(route_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)smem);
+  if (e != cudaSuccess) return e;
+  return launch_kernel(route_fused_kernel, dim3((s.T + TOK - 1) / TOK), dim3(NUM_THREADS), smem,
+                       stream, pdl, mX, mW, f);
+}
+
+}  // namespace moe

@@ -43,231 +43,15 @@
 #include "common.cuh"
 #include "expert_layout.cuh"
 #include "internal.h"
+#include "route_finish.cuh"
 
 namespace moe {
 namespace {
 
+using namespace route;
+
 constexpr int WARPS = SELECT_WARPS;  // 32
 constexpr int MAX_TPW = 4;           // tokens per warp whose ranks stay in registers
-
-__device__ __forceinline__ float warp_max(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-  return v;
-}
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
-}
-__device__ __forceinline__ double warp_sum(double v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
-}
-
-// Exclusive prefix of v over the 1024 threads of the block, in thread order; *total
-// gets the sum. s_w: 32 ints of shared memory. Contains __syncthreads.
-__device__ int block_exclusive_scan(int v, int32_t* s_w, int* total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int x = v;
-#pragma unroll
-  for (int d = 1; d < 32; d <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, x, d);
-    if (lane >= d) x += y;
-  }
-  if (lane == 31) s_w[warp] = x;
-  __syncthreads();
-  if (warp == 0) {
-    int w = s_w[lane];
-#pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, w, d);
-      if (lane >= d) w += y;
-    }
-    s_w[lane] = w;
-  }
-  __syncthreads();
-  const int before = (warp > 0 ? s_w[warp - 1] : 0) + x - v;
-  *total = s_w[31];
-  __syncthreads();
-  return before;
-}
-
-// Sum of v over the block in a fixed order (deterministic). s_d: 32 doubles.
-__device__ double block_sum(double v, double* s_d) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  v = warp_sum(v);
-  if (lane == 0) s_d[warp] = v;
-  __syncthreads();
-  double r = warp_sum(lane < 32 ? s_d[lane] : 0.0);
-  __syncthreads();
-  return r;
-}
-
-// The last block's scan (1024 threads). Thread (g, col) walks a contiguous range of
-// block rows of one expert column; a warp covers consecutive columns of the same rows,
-// so its loads are coalesced. A parallel prefix over the row groups gives every group
-// its base, and warp 0 scans the experts for offsets and tile starts.
-__device__ void finish_routing(const SelectArgs& a, int nblk) {
-  __shared__ int32_t ip[1024];
-  __shared__ float fq[1024];
-  __shared__ int32_t s_counts[MAX_EXPERTS], s_kept[MAX_EXPERTS];
-  __shared__ float s_psum[256];
-  __shared__ int32_t s_w[32];
-  __shared__ double s_d[32];
-  const int tid = threadIdx.x;
-  const int N = a.N, Ntot = a.N + a.S;
-  // Valid tokens: per-block counts -> exclusive bases, and their total.
-  int T_valid = a.T;
-  if (a.valid != nullptr) {
-    const int R = (nblk + 1023) / 1024;
-    const int b0 = min(nblk, tid * R), b1 = min(nblk, b0 + R);
-    int mine = 0;
-    for (int b = b0; b < b1; ++b) mine += a.blk_valid[b];
-    int run = block_exclusive_scan(mine, s_w, &T_valid);
-    for (int b = b0; b < b1; ++b) {
-      const int c = a.blk_valid[b];
-      a.blk_valid[b] = run;
-      run += c;
-    }
-  }
-  // Capacity of this call: C = ceil(CF * T_valid * k / N) in double, at most T_valid*k
-  // (the host's value when every token is valid). One thread evaluates it (fp64 is
-  // slow on this part) and shares it; the first read comes after the barrier that
-  // follows the column sums below.
-  __shared__ long long s_C;
-  if (tid == 0) {
-    long long C = a.C;
-    if (a.valid != nullptr && a.cf > 0.0) {
-      const double c = ceil(a.cf * (double)T_valid * (double)a.k / (double)N);
-      const double slots = (double)T_valid * (double)a.k;
-      C = c >= slots ? (long long)slots : (long long)c;
-    }
-    s_C = C;
-    *a.cap = (int32_t)C;
-  }
-  double d2 = 0.0;  // sum of (P - 1/N)^2 over the valid tokens
-  if (a.aux_std2 != nullptr) {
-    const int R = (nblk + 1023) / 1024;
-    const int b0 = min(nblk, tid * R), b1 = min(nblk, b0 + R);
-    double mine = 0.0;
-    for (int b = b0; b < b1; ++b) mine += (double)a.blk_d2[b];
-    d2 = block_sum(mine, s_d);
-  }
-  int np2 = 1;
-  while (np2 < N) np2 <<= 1;
-  const int G = 1024 / np2;                 // row groups
-  const int col = tid % np2, g = tid / np2;
-  const int R = (nblk + G - 1) / G;
-  const int r0 = min(nblk, g * R), r1 = min(nblk, r0 + R);
-  constexpr int B = 8;                      // rows per batch: B loads in flight per thread
-  int isum = 0;
-  float fsum = 0.f;
-  if (col < N) {
-    for (int rb = r0; rb < r1; rb += B) {
-      int iv[B];
-      float fv[B];
-#pragma unroll
-      for (int u = 0; u < B; ++u) {
-        const bool in = rb + u < r1;
-        iv[u] = in ? a.blk_counts[(size_t)(rb + u) * N + col] : 0;
-        fv[u] = in ? a.blk_psum[(size_t)(rb + u) * N + col] : 0.f;
-      }
-#pragma unroll
-      for (int u = 0; u < B; ++u) {
-        isum += iv[u];
-        fsum += fv[u];
-      }
-    }
-  }
-  ip[tid] = isum;
-  fq[tid] = fsum;
-  __syncthreads();
-  // inclusive prefix over the row groups of each column (fixed pattern: deterministic)
-  for (int d = 1; d < G; d <<= 1) {
-    const int iv = g >= d ? ip[tid - d * np2] : 0;
-    const float fv = g >= d ? fq[tid - d * np2] : 0.f;
-    __syncthreads();
-    ip[tid] += iv;
-    fq[tid] += fv;
-    __syncthreads();
-  }
-  const long long C = s_C;
-  if (col < N && g == G - 1) {
-    const int run = ip[tid];
-    const int kept = (C < 0 || (long long)run <= C) ? run : (int)C;
-    s_counts[col] = run;
-    s_kept[col] = kept;
-    s_psum[col] = fq[tid];
-    a.counts[col] = run;
-    a.kept[col] = kept;
-    if (a.user_counts != nullptr) a.user_counts[col] = run;
-    if (a.user_kept != nullptr) a.user_kept[col] = kept;
-  }
-  if (tid < a.S) {  // shared experts take every valid token, no capacity
-    s_counts[N + tid] = T_valid;
-    s_kept[N + tid] = T_valid;
-    a.counts[N + tid] = T_valid;
-    a.kept[N + tid] = T_valid;
-  }
-  if (col < N) {  // exclusive per-expert base of every block
-    int run = ip[tid] - isum;
-    for (int rb = r0; rb < r1; rb += B) {
-      int iv[B];
-#pragma unroll
-      for (int u = 0; u < B; ++u)
-        iv[u] = rb + u < r1 ? a.blk_counts[(size_t)(rb + u) * N + col] : 0;
-#pragma unroll
-      for (int u = 0; u < B; ++u) {
-        if (rb + u < r1) a.blk_counts[(size_t)(rb + u) * N + col] = run;
-        run += iv[u];
-      }
-    }
-  }
-  __syncthreads();
-  if (tid < 32) {  // warp 0: the losses over the routed experts
-    const int lane = tid;
-    float fp = 0.f;
-    double lsum = 0.0;
-    int empty = 0;
-    for (int e = lane; e < N; e += 32) {
-      fp = fmaf((float)s_counts[e], s_psum[e], fp);
-      if (a.aux_kl != nullptr) {
-        if (s_counts[e] == 0) empty = 1;
-        else lsum += log((double)N * (double)s_counts[e] / ((double)T_valid * (double)a.k));
-      }
-    }
-#pragma unroll
-    for (int d = 16; d > 0; d >>= 1) fp += __shfl_xor_sync(0xffffffffu, fp, d);
-    if (a.aux_kl != nullptr) {
-      lsum = warp_sum(lsum);
-      empty = __any_sync(0xffffffffu, empty);
-    }
-    if (lane == 0) {
-      // aux = N * sum_e (counts_e / (T*k)) * (Psum_e / T), T the valid tokens;
-      // counts <= T*k and sum_e Psum_e = T keep every term well inside fp32 range
-      const float Tf = (float)T_valid;
-      *a.aux = T_valid > 0 ? (float)N * (fp / (Tf * (float)a.k)) / Tf : 0.f;
-      // KL(uniform || f) = -(1/N) sum_e log(N f_e); +inf when an expert got nothing
-      if (a.aux_kl != nullptr)
-        *a.aux_kl = T_valid == 0 ? 0.f : empty ? INFINITY : (float)(-lsum / (double)N);
-      // unbiased variance of the T_valid*N probabilities around their mean 1/N
-      if (a.aux_std2 != nullptr)
-        *a.aux_std2 =
-            T_valid == 0 ? 0.f : (float)(d2 / ((double)T_valid * (double)N - 1.0));
-    }
-  }
-  ExpertLayout lay;
-  lay.offsets = a.offsets;
-  for (int tb = 0; tb < 2; ++tb) {
-    lay.tile_first[tb] = a.tile_first[tb];
-    lay.num_mtiles[tb] = a.num_mtiles[tb];
-    lay.tile_expert[tb] = a.tile_expert[tb];
-    lay.tile_row0[tb] = a.tile_row0[tb];
-  }
-  layout_experts(s_kept, Ntot, lay);
-}
 
 // OPT: the valid-token mask or the variance loss may be in use (read at run time);
 // without it those branches are compiled out of the base layer's kernel.
@@ -279,12 +63,16 @@ __global__ void __launch_bounds__(1024) route_select_kernel(SelectArgs a) {
   __shared__ int is_last;
   __shared__ int32_t s_vbase[WARPS];   // valid tokens before each warp's range
   __shared__ float s_d2[WARPS];
+  __shared__ float s_bias[256];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int N = a.N, k = a.k;
   for (int i = threadIdx.x; i < WARPS * N; i += blockDim.x) {
     cnt[i] = 0;
     pw[i] = 0.f;
   }
+  // the bias is the caller's input, not a predecessor's output: read before the wait
+  if (a.bias != nullptr)
+    for (int i = threadIdx.x; i < N; i += blockDim.x) s_bias[i] = a.bias[i];
   pdl_wait();  // partial logits come from the router kernel
   pdl_trigger();
   const int NI = (N + 31) >> 5;  // experts per lane, <= 8
@@ -350,7 +138,7 @@ __global__ void __launch_bounds__(1024) route_select_kernel(SelectArgs a) {
     if (a.bias != nullptr) {
 #pragma unroll
       for (int q = 0; q < 8; ++q)
-        if (q < NI && lane + 32 * q < N) v[q] += a.bias[lane + 32 * q];
+        if (q < NI && lane + 32 * q < N) v[q] += s_bias[lane + 32 * q];
     }
     // softmax over all N experts
     float m = -INFINITY;

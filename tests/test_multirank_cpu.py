@@ -83,3 +83,18 @@ def test_algorithmic_units_match_hand_counts():
     d = configs.DECODE_T64  # 128 slots over 75 experts: weight streaming, ~1 FLOP/B
     ud = bench.algorithmic_units(d, kept_slots=128, touched_experts=75)
     assert bench.bound_of(*ud["gemm1_swiglu"], peaks) == "hbm"
+
+
+def test_stage_names_and_launch_counts():
+    sys.path.insert(0, ROOT)
+    import bench
+    from mixture_experts_layer_102_b300 import configs
+    bf = configs.BF16_T4096
+    f32 = configs.TINY_F32
+    assert bench.stage_names(bf) == ["route", "dispatch", "gemm1_swiglu", "gemm2", "combine"]
+    assert bench.stage_names(f32) == bench.STAGES
+    assert bench.stage_names(configs.DECODE_T64) == bench.STAGES     # 1 tile: split router
+    assert bench.launches_per_forward(bf) == 5 and bench.launches_per_forward(f32) == 6
+    u = bench.algorithmic_units(bf, kept_slots=8192, touched_experts=16)
+    assert u["route"][0] == u["router_logits"][0]
+    assert u["route"][1] == u["router_logits"][1] + u["route_select"][1]
