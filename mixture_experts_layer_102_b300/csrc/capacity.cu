@@ -60,10 +60,14 @@ __global__ void __launch_bounds__(256) dispatch_kernel(DispatchArgs a) {
         report(a.status, STATUS_BAD_INDEX);
         a.drop[j] = 1;
       } else {
-        const long long rank = (long long)a.blk_base[(size_t)blk * a.N + e] + a.slot_rank[j];
+        // base, in-block rank and offset are independent loads: one round trip
+        const int base = a.blk_base[(size_t)blk * a.N + e];
+        const int srank = a.slot_rank[j];
+        const int off = a.offsets[e];
+        const long long rank = (long long)base + srank;
         bool kept = C < 0 || rank < C;
         if (kept) {
-          row = a.offsets[e] + (int)rank;
+          row = off + (int)rank;
         } else if (a.rr_exp != nullptr) {  // rerouted: after the new expert's own rows
           const int c = a.rr_exp[j];
           if (c >= 0 && c < a.N) {

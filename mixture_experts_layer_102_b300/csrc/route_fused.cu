@@ -229,8 +229,10 @@ route_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
     s_valid[r] = live ? 1 : 0;
     if (live) {
       float m = -INFINITY;
+#pragma unroll 8
       for (int e = 0; e < N; ++e) m = fmaxf(m, row[e]);
       float sum = 0.f;
+#pragma unroll 8
       for (int e = 0; e < N; ++e) sum += expf(row[e] - m);
       const float inv = 1.f / sum;
       // top k: pick j is the best logit strictly after pick j-1 in (logit desc, id asc)
@@ -239,6 +241,7 @@ route_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
       for (int j = 0; j < k; ++j) {
         float bv = -INFINITY;
         int bi = -1;
+#pragma unroll 8
         for (int e = 0; e < N; ++e) {
           const float v = row[e];
           const bool after = v < pl || (v == pl && e > pi);
@@ -264,6 +267,7 @@ route_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
         ch[e] = (uint8_t)(j + 1);
       }
       const float invN = 1.f / (float)N;
+#pragma unroll 8
       for (int e = 0; e < N; ++e) {  // the token's probabilities replace its logits
         const float pe = expf(row[e] - m) * inv;
         row[e] = pe;
