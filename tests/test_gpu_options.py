@@ -162,7 +162,14 @@ def check_opts(cfg, n_shared=0, activation="swiglu", seq_len=None, token_sample=
 
 
 # (workload, shared experts, activation, sequence length of the padding mask or None)
+# bf16 layers of 32 or more tiles of 128 tokens run the fused router + routing kernel
 CASES = [
+    (MoEConfig("bf16_fused_n256_k8_t4000", 4000, 128, 256, 8, 64, 1.5, "bf16", seed=38), 0,
+     "swiglu", None),
+    (MoEConfig("bf16_fused_n1_k1_t4096", 4096, 128, 1, 1, 64, None, "bf16", seed=39), 0,
+     "swiglu", None),
+    (MoEConfig("bf16_fused_k32_n64_masked_shared", 4100, 64, 64, 32, 64, 0.9, "bf16", seed=40,
+               zipf_bias=True), 2, "gelu", 300),
     (configs.TINY_F32.with_(name="f32_shared2_tight", capacity_factor=0.6), 2, "swiglu", None),
     (configs.TINY_F32.with_(name="f32_gelu"), 0, "gelu", None),
     (configs.TINY_F32.with_(name="f32_masked", capacity_factor=1.0), 0, "swiglu", 16),
