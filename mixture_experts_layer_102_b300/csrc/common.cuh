@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+
 namespace moe {
 
 // Bits a kernel ORs into the workspace status word.
@@ -47,6 +49,54 @@ inline cudaError_t launch_kernel(void (*kernel)(Exp...), dim3 grid, dim3 block, 
   cfg.numAttrs = pdl ? 1 : 0;
   const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, static_cast<Act&&>(args)...);
   return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+// Let `kernel` use `bytes` of dynamic shared memory on the current device. The
+// attribute is set once per kernel and device (and again only to raise it), so
+// launches do not pay a driver call each time; safe to call from several threads.
+inline cudaError_t ensure_dynamic_smem(const void* kernel, size_t bytes) {
+  struct Entry {
+    const void* fn;
+    int dev;
+    size_t bytes;
+  };
+  static std::mutex mu;
+  static Entry table[256];
+  static int used = 0;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  int slot = -1;
+  for (int i = 0; i < used; ++i)
+    if (table[i].fn == kernel && table[i].dev == dev) {
+      if (table[i].bytes >= bytes) return cudaSuccess;
+      slot = i;
+      break;
+    }
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e != cudaSuccess) return e;
+  if (slot < 0 && used < 256) slot = used++;
+  if (slot >= 0) table[slot] = Entry{kernel, dev, bytes};
+  return cudaSuccess;
+}
+
+// Opt-in shared memory per block of the current device (cached per device).
+inline cudaError_t smem_optin_bytes(size_t* out) {
+  static int cached[64] = {0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < 64 && cached[dev] > 0) {
+    *out = (size_t)cached[dev];
+    return cudaSuccess;
+  }
+  int v = 0;
+  e = cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < 64) cached[dev] = v;
+  *out = (size_t)v;
+  return cudaSuccess;
 }
 
 __device__ __forceinline__ float bf16_lo(uint32_t u) { return __uint_as_float(u << 16); }

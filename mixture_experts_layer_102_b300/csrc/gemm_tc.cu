@@ -434,9 +434,8 @@ int grid_units() {
 template <int EPI, int CG>
 cudaError_t launch_t(const CUtensorMap& mA, const CUtensorMap& mB0, const CUtensorMap& mB1,
                      const TcArgs& t, cudaStream_t stream, bool pdl) {
-  cudaError_t e = cudaFuncSetAttribute(grouped_gemm_tc_kernel<EPI, CG>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)Shape<CG>::SMEM_BYTES);
+  cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(grouped_gemm_tc_kernel<EPI, CG>),
+                                      Shape<CG>::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(CG * grid_units<EPI, CG>(), 1, 1);

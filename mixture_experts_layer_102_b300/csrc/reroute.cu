@@ -175,8 +175,7 @@ __global__ void __launch_bounds__(1024) reroute_kernel(RerouteArgs a) {
 cudaError_t launch_reroute(const RerouteArgs& a, int nblk, cudaStream_t stream, bool pdl) {
   if (a.T == 0) return cudaSuccess;
   const size_t smem = (size_t)WARPS * a.N * 4;
-  const cudaError_t e = cudaFuncSetAttribute(
-      reroute_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  const cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(reroute_kernel), smem);
   if (e != cudaSuccess) return e;
   return launch_kernel(reroute_kernel, dim3(nblk), dim3(WARPS * 32), smem, stream, pdl, a);
 }

@@ -45,7 +45,6 @@ constexpr int TOK = 128;                        // tokens per CTA (TMEM lanes)
 constexpr uint32_t A_BYTES = TOK * BK * 2;      // 16 KB
 constexpr int NUM_THREADS = 256;
 constexpr int MAX_STAGES = 16;
-constexpr int SMEM_OPTIN = 232448;              // bytes of shared memory per block
 
 struct FusedArgs {
   SelectArgs s;        // outputs, options and workspace arrays of the routing decisions
@@ -372,12 +371,24 @@ cudaError_t launch_route_fused(const SelectArgs& s, const void* x, const void* w
   // kind::f16 descriptor: D fp32, A/B bf16, K-major, N = n_pad, M = 128
   f.idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(f.n_pad >> 3) << 17) |
             ((uint32_t)(TOK >> 4) << 24);
-  cudaFuncAttributes attr;
-  cudaError_t e = cudaFuncGetAttributes(&attr, route_fused_kernel);
+  // the kernel's static shared memory (once per process: it does not depend on the
+  // device) and the device's opt-in limit bound the dynamic part
+  static size_t static_smem = 0;
+  static std::once_flag once;
+  cudaError_t e = cudaSuccess;
+  std::call_once(once, [&] {
+    cudaFuncAttributes attr;
+    e = cudaFuncGetAttributes(&attr, route_fused_kernel);
+    static_smem = attr.sharedSizeBytes;
+  });
+  if (e != cudaSuccess || static_smem == 0) return e != cudaSuccess ? e : cudaErrorInvalidValue;
+  size_t optin = 0;
+  e = smem_optin_bytes(&optin);
   if (e != cudaSuccess) return e;
   const size_t epi = (size_t)TOK * (s.N + 1) * 4 + (size_t)TOK * s.k * 4 + (size_t)TOK * s.N;
   const size_t tail = 8 * (2 * MAX_STAGES + 1) + 16;  // barriers, TMEM address, abort flag
-  const size_t avail = (size_t)SMEM_OPTIN - attr.sharedSizeBytes - 1024 - tail;
+  if (optin < static_smem + 1024 + tail) return cudaErrorInvalidValue;
+  const size_t avail = optin - static_smem - 1024 - tail;
   int stages = (int)(avail / f.stage_bytes);
   if (stages > MAX_STAGES) stages = MAX_STAGES;
   if (stages > f.kc_total) stages = f.kc_total > 1 ? f.kc_total : 1;
@@ -392,8 +403,7 @@ cudaError_t launch_route_fused(const SelectArgs& s, const void* x, const void* w
   if (!make_map(&mX, x, 2, (uint64_t)H, 0, (uint64_t)s.T, TOK)) return cudaErrorInvalidValue;
   if (!make_map(&mW, w_router, 2, (uint64_t)H, 0, (uint64_t)s.N, (uint32_t)f.n_pad))
     return cudaErrorInvalidValue;
-  e = cudaFuncSetAttribute(route_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)smem);
+  e = ensure_dynamic_smem(reinterpret_cast<const void*>(route_fused_kernel), smem);
   if (e != cudaSuccess) return e;
   return launch_kernel(route_fused_kernel, dim3((s.T + TOK - 1) / TOK), dim3(NUM_THREADS), smem,
                        stream, pdl, mX, mW, f);

@@ -275,8 +275,7 @@ cudaError_t launch_route_select(const SelectArgs& a, int nblk, cudaStream_t stre
   const size_t smem = (size_t)WARPS * a.N * 8;  // counters and P sums of every warp
   const bool opt = a.valid != nullptr || a.aux_std2 != nullptr;
   auto kernel = opt ? route_select_kernel<true> : route_select_kernel<false>;
-  const cudaError_t e =
-      cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  const cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(kernel), smem);
   if (e != cudaSuccess) return e;
   return launch_kernel(kernel, dim3(nblk), dim3(WARPS * 32), smem, stream, pdl, a);
 }

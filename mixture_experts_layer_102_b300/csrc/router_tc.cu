@@ -216,8 +216,7 @@ cudaError_t launch_router_logits_tc(const void* x, const void* w_router, float* 
   a.stage_bytes = (A_BYTES + a.b_bytes + 1023u) & ~1023u;
   a.status = status;
   const size_t smem = 1024 + (size_t)STAGES * a.stage_bytes + 256;
-  const cudaError_t e = cudaFuncSetAttribute(
-      router_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  const cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(router_tc_kernel), smem);
   if (e != cudaSuccess) return e;
   return launch_kernel(router_tc_kernel, dim3((T + 127) / 128, ksplit), dim3(NUM_THREADS), smem,
                        stream, pdl, mX, mW, a);
