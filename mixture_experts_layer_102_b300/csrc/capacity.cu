@@ -30,22 +30,24 @@ __global__ void __launch_bounds__(256) dispatch_kernel(DispatchArgs a) {
   __shared__ int32_t rows[8][MAX_SLOTS];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * 8 + warp;
-  pdl_wait();  // ranks, bases and offsets come from the routing-decision kernel
-  pdl_trigger();
-  if (t >= a.T) return;
-  // The token's first VPL x vectors per lane are requested before the chain of
-  // dependent index loads below, so the two overlap.
+  // The token's first VPL x vectors per lane are requested before the wait (x is the
+  // caller's input) and before the chain of dependent index loads below.
   constexpr int VPL = 8;
-  const uint4* src = reinterpret_cast<const uint4*>(static_cast<const TIn*>(a.x) + (size_t)t * a.H);
+  const bool live = t < a.T;
+  const uint4* src = reinterpret_cast<const uint4*>(static_cast<const TIn*>(a.x) +
+                                                    (size_t)(live ? t : 0) * a.H);
   const int nvec = a.H * (int)sizeof(TIn) / 16;
   uint4 val[VPL];
-  if (COPY) {
+  if (COPY && live) {
 #pragma unroll
     for (int u = 0; u < VPL; ++u) {
       const int v = u * 32 + lane;
       if (v < nvec) val[u] = src[v];
     }
   }
+  pdl_wait();  // ranks, bases and offsets come from the routing-decision kernel
+  pdl_trigger();
+  if (!live) return;
   const int slots = a.k + a.S;
   const long long C = a.valid != nullptr ? (long long)*a.cap : a.C;
   const int blk = t / a.tokens_per_block;

@@ -25,14 +25,18 @@ combine_kernel(const TIo* __restrict__ ye, const int32_t* __restrict__ slot_row,
   __shared__ float wts[8][MAX_SLOTS];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * 8 + warp;
+  const int slots = k + S;
+  // slot_row and w come from dispatch and the routing kernels, which had completed
+  // before the second expert GEMM let this kernel start (that GEMM triggers only after
+  // its own wait on the first, which waited on dispatch): read before the wait
+  if (t < T)
+    for (int sl = lane; sl < slots; sl += 32) {
+      rows[warp][sl] = slot_row[(size_t)t * slots + sl];
+      wts[warp][sl] = sl < k ? w[(size_t)t * k + sl] : 1.f;
+    }
   pdl_wait();  // ye comes from the second expert GEMM
   pdl_trigger();
   if (t >= T) return;
-  const int slots = k + S;
-  for (int sl = lane; sl < slots; sl += 32) {
-    rows[warp][sl] = slot_row[(size_t)t * slots + sl];
-    wts[warp][sl] = sl < k ? w[(size_t)t * k + sl] : 1.f;
-  }
   __syncwarp();
   // Groups of 8 elements (one 16-byte bf16 vector); each lane keeps VPL groups in
   // flight per slot so the loads of a slot overlap.

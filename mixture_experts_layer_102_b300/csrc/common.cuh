@@ -25,8 +25,10 @@ __device__ __forceinline__ void report(uint32_t* status, uint32_t bits) {
 // launched as a dependent). pdl_trigger: let the next kernel of the stream start
 // launching. Every kernel here calls both, in that order, after a prologue that reads
 // at most the caller's own inputs (complete before the forward's first kernel, which
-// is never a dependent launch, started), so at most two adjacent kernels overlap and
-// all blocks of the earlier one are already resident when the later one starts.
+// is never a dependent launch, started) or the outputs of kernels two or more launches
+// back (complete before the previous kernel, which triggers only after its own wait,
+// let this one start), so at most two adjacent kernels overlap and all blocks of the
+// earlier one are already resident when the later one starts.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
