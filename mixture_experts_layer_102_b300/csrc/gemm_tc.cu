@@ -181,21 +181,24 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
       asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
   }
-  tc_fence_before();
-  if constexpr (CG == 2) cluster_sync();  // both CTAs' barriers and TMEM ready
-  else __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem_base = static_cast<uint32_t>(misc[0]);
-  pdl_wait();  // tile tables and the A rows come from earlier kernels
-  pdl_trigger();
-
+  // The expert layout comes from the routing kernels, which ran two or more launches
+  // before this one and have completed; only the A rows (the previous kernel's output)
+  // need the wait below.
   __shared__ int32_t tfirst[MAX_EXPERTS + 1], roff[MAX_EXPERTS + 1];
   for (int i = threadIdx.x; i <= a.N; i += blockDim.x) {
     tfirst[i] = a.tile_first[i];
     roff[i] = a.offsets[i];
   }
-  __syncthreads();
+  tc_fence_before();
+  if constexpr (CG == 2) cluster_sync();  // both CTAs' barriers, TMEM and tables ready
+  else __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = static_cast<uint32_t>(misc[0]);
   const int num_mt = *a.num_mtiles;
+  if (threadIdx.x != 0) {  // the producer (thread 0) waits after its first weight loads
+    pdl_wait();
+    pdl_trigger();
+  }
   const int total = num_mt * a.n_tiles;
   const int kchunks = a.K / BK;
   const int unit = blockIdx.x / CG;       // CTA (CG = 1) or CTA pair (CG = 2)
@@ -205,7 +208,32 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
     if (lane == 0) {  // ---------------------------------------------- TMA producer
       // CG = 2: both CTAs' loads complete on the first CTA's full barriers.
       const uint32_t full_c = CG == 2 ? map_to_cta(full_bar, 0) : full_bar;
-      int stage = 0;
+      // Weight boxes of k-chunk kc of expert e, column tile n0, into stage sA.
+      auto load_b = [&](uint32_t sA, uint32_t fb, int kc, int n0, int e) {
+        if constexpr (CG == 2) {
+          if (leader) tma_load_3d<CG>(sA + BOX_BYTES, &tmB0, fb, kc * BK, n0, e);
+          else tma_load_3d<CG>(sA + BOX_BYTES, &tmB1, fb, kc * BK, n0 + a.b1_row_off, e);
+        } else {
+          tma_load_3d<CG>(sA + BOX_BYTES, &tmB0, fb, kc * BK, n0, e);
+          tma_load_3d<CG>(sA + 2 * BOX_BYTES, &tmB1, fb, kc * BK, n0 + a.b1_row_off, e);
+        }
+      };
+      // The weights are the caller's: the first unit's weight boxes for the first
+      // STAGES k-chunks go out before the wait for the previous kernel (the stages are
+      // fresh, so no empty-barrier wait is due), and only their A boxes follow it.
+      int pre = 0;
+      if (unit < total) {
+        int e, mt, nt;
+        raster(unit, tfirst, a.N, a.n_tiles, e, mt, nt);
+        pre = min(S::STAGES, kchunks);
+        for (int kc = 0; kc < pre; ++kc) {
+          if (leader) mbar_expect_tx(full_bar + 8 * kc, CG * S::STAGE_BYTES);
+          load_b(base + kc * S::STAGE_BYTES, full_c + 8 * kc, kc, nt * a.n_per_tile, e);
+        }
+      }
+      pdl_wait();
+      pdl_trigger();
+      int stage = 0, issued = 0;
       uint32_t phase = 0;
       uint32_t used = 0, last_parity = 0;
       bool ok = true;
@@ -214,22 +242,18 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
         raster(w, tfirst, a.N, a.n_tiles, e, mt, nt);
         const int row0 = roff[e] + (mt - tfirst[e]) * S::TILE_M + (int)rank * 128;
         const int n0 = nt * a.n_per_tile;
-        for (int kc = 0; kc < kchunks; ++kc) {
-          if (!mbar_wait(empty_bar + 8 * stage, phase ^ 1u, abort_flag, WAIT_LIMIT_NS)) {
-            ok = false;
-            break;
-          }
+        for (int kc = 0; kc < kchunks; ++kc, ++issued) {
           const uint32_t sA = base + stage * S::STAGE_BYTES;
           const uint32_t fb = full_c + 8 * stage;
-          if (leader) mbar_expect_tx(full_bar + 8 * stage, CG * S::STAGE_BYTES);
-          tma_load_2d<CG>(sA, &tmA, fb, kc * BK, row0);
-          if constexpr (CG == 2) {
-            if (leader) tma_load_3d<CG>(sA + BOX_BYTES, &tmB0, fb, kc * BK, n0, e);
-            else tma_load_3d<CG>(sA + BOX_BYTES, &tmB1, fb, kc * BK, n0 + a.b1_row_off, e);
-          } else {
-            tma_load_3d<CG>(sA + BOX_BYTES, &tmB0, fb, kc * BK, n0, e);
-            tma_load_3d<CG>(sA + 2 * BOX_BYTES, &tmB1, fb, kc * BK, n0 + a.b1_row_off, e);
+          if (issued >= pre) {
+            if (!mbar_wait(empty_bar + 8 * stage, phase ^ 1u, abort_flag, WAIT_LIMIT_NS)) {
+              ok = false;
+              break;
+            }
+            if (leader) mbar_expect_tx(full_bar + 8 * stage, CG * S::STAGE_BYTES);
+            load_b(sA, fb, kc, n0, e);
           }
+          tma_load_2d<CG>(sA, &tmA, fb, kc * BK, row0);
           used |= 1u << stage;
           last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
           if (++stage == S::STAGES) {
