@@ -39,6 +39,9 @@ from mixture_experts_layer_102_b300 import configs, inputs  # noqa: E402
 
 METRIC = "MoE layer fwd tokens/s; grouped-GEMM TFLOP/s and routing GB/s as % of B300 peak"
 UNIT = "tokens/s"
+# Buffer sets of the pipelined end-to-end loop: with three, the copy-in of a step
+# waits for the forward three steps back, not for the one just before it.
+E2E_BUFFERS = 3
 DEFAULT_CONFIG = configs.BF16_T4096
 FLUSH_BYTES = 256 << 20
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
@@ -356,36 +359,38 @@ def run_gpu_arm(args, cfg):
     # memory to the device and its out and aux back to pinned host memory. Pipelined
     # as a serving loop would run it: the copy-in of step i+1 and the copy-out of step
     # i run on their own streams beside the forward of step i (double buffers ordered
-    # by events). The fully serial loop (copy, forward, copy, synchronise) is also
-    # reported.
+    # by events; E2E_BUFFERS sets of buffers, so a forward waits only on the copies of
+    # the step E2E_BUFFERS back). The fully serial loop (copy, forward, copy,
+    # synchronise) is also reported.
     e2e = None
     if not args.no_e2e:
         n_e2e = min(args.steps, 200)
         b = 2 if cfg.dtype == "bf16" else 4
+        nb = E2E_BUFFERS
         x_host = [moe.to_torch(inputs.make_x(cfg, rank=rank * 7919 + 1 + j), cfg.dtype).pin_memory()
-                  for j in range(2)]
-        out_host = [torch.empty((cfg.T, cfg.H), dtype=dev.x.dtype).pin_memory() for _ in range(2)]
-        aux_host = [torch.empty(1, dtype=torch.float32).pin_memory() for _ in range(2)]
-        x_dev = [torch.empty_like(dev.x) for _ in range(2)]
-        out_dev = [torch.empty_like(out) for _ in range(2)]
-        rts = [moe.new_routing(c, device) for _ in range(2)]
+                  for j in range(nb)]
+        out_host = [torch.empty((cfg.T, cfg.H), dtype=dev.x.dtype).pin_memory() for _ in range(nb)]
+        aux_host = [torch.empty(1, dtype=torch.float32).pin_memory() for _ in range(nb)]
+        x_dev = [torch.empty_like(dev.x) for _ in range(nb)]
+        out_dev = [torch.empty_like(out) for _ in range(nb)]
+        rts = [moe.new_routing(c, device) for _ in range(nb)]
         s_in = torch.cuda.Stream(device)
         s_out = torch.cuda.Stream(device)
-        ev_in = [torch.cuda.Event() for _ in range(2)]
-        ev_fwd = [torch.cuda.Event() for _ in range(2)]
-        ev_out = [torch.cuda.Event() for _ in range(2)]
+        ev_in = [torch.cuda.Event() for _ in range(nb)]
+        ev_fwd = [torch.cuda.Event() for _ in range(nb)]
+        ev_out = [torch.cuda.Event() for _ in range(nb)]
 
         def run_pipelined(n):
             for i in range(n):
-                j = i % 2
+                j = i % nb
                 with torch.cuda.stream(s_in):
-                    if i >= 2:
-                        s_in.wait_event(ev_fwd[j])        # step i-2 no longer reads x_dev[j]
+                    if i >= nb:
+                        s_in.wait_event(ev_fwd[j])        # step i-nb no longer reads x_dev[j]
                     x_dev[j].copy_(x_host[j], non_blocking=True)
                     ev_in[j].record(s_in)
                 stream.wait_event(ev_in[j])
-                if i >= 2:
-                    stream.wait_event(ev_out[j])          # step i-2's out has been copied out
+                if i >= nb:
+                    stream.wait_event(ev_out[j])          # step i-nb's out has been copied out
                 moe.forward(c, x_dev[j], dev.w_router, dev.router_bias, dev.w1, dev.w3, dev.w2,
                             workspace=ws, out=out_dev[j], routing=rts[j], stream=stream)
                 ev_fwd[j].record(stream)
@@ -398,7 +403,7 @@ def run_gpu_arm(args, cfg):
 
         def run_serial(n):
             for i in range(n):
-                j = i % 2
+                j = i % nb
                 x_dev[j].copy_(x_host[j], non_blocking=True)
                 moe.forward(c, x_dev[j], dev.w_router, dev.router_bias, dev.w1, dev.w3, dev.w2,
                             workspace=ws, out=out_dev[j], routing=rts[j], stream=stream)
@@ -421,8 +426,8 @@ def run_gpu_arm(args, cfg):
                "h2d_bytes_per_step": cfg.T * cfg.H * b,
                "d2h_bytes_per_step": cfg.T * cfg.H * b + 4,
                "ms_per_step": round(pipe_s * 1e3, 5), "steps": n_e2e,
-               "mode": "pipelined: copy-in of step i+1 and copy-out of step i on their "
-                       "own streams beside the forward of step i",
+               "mode": f"pipelined: copy-in of step i+1 and copy-out of step i on their "
+                       f"own streams beside the forward of step i, {nb} buffer sets",
                "serial_value": round(total_tokens / serial_s, 1),
                "serial_ms_per_step": round(serial_s * 1e3, 5)}
 
