@@ -17,11 +17,12 @@
 //   warp 1      TMEM allocator; one thread issues tcgen05.mma.cta_group::1 (M=128,
 //               N=N_pad, K=16) into a TMEM accumulator.
 //   warps 2-5   read the accumulator back (one token per thread: the TMEM lane) and
-//               stage the logits (+ bias) in the freed stage memory; then each thread
-//               makes its token's decisions: softmax by max and sum, the top k by k
-//               passes, each taking the best logit strictly after the previous pick in
-//               the order (logit descending, id ascending), the gate weights, and the
-//               token's row of probabilities.
+//               stage the logits (+ bias) in the freed stage memory.
+//   all warps   two threads per token (experts of one parity each, combined by
+//               shuffles) make the token's decisions: softmax by max and sum, the top k
+//               by k passes, each taking the best logit strictly after the previous
+//               pick in the order (logit descending, id ascending), the gate weights,
+//               and the token's row of probabilities.
 //   all warps   per expert, in a fixed order over the tile's rows: the sum of P, the
 //               count, and each slot's rank among the tile's earlier slots of that
 //               expert (its rank in token order inside the tile).
@@ -45,6 +46,13 @@ constexpr int TOK = 128;                        // tokens per CTA (TMEM lanes)
 constexpr uint32_t A_BYTES = TOK * BK * 2;      // 16 KB
 constexpr int NUM_THREADS = 256;
 constexpr int MAX_STAGES = 16;
+
+// Row stride (floats) of the tile's logits in shared memory: at least N + 1 and 2 mod 4,
+// so the two threads of each of a warp's 16 tokens (experts of one parity each) fall
+// in 32 different banks.
+__host__ __device__ constexpr int logit_stride(int N) {
+  return (N + 1) % 4 == 2 ? N + 1 : (N + 2) % 4 == 2 ? N + 2 : (N + 3) % 4 == 2 ? N + 3 : N + 4;
+}
 
 struct FusedArgs {
   SelectArgs s;        // outputs, options and workspace arrays of the routing decisions
@@ -167,14 +175,13 @@ route_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
   }
   // Epilogue shared memory, in the stage region (every load has landed and every MMA
   // has read its operands once the accumulator barrier flips):
-  //   L  [TOK][N+1] logits, then probabilities     (fp32)
+  //   L  [TOK][LS]  logits, then probabilities     (fp32, LS = logit_stride(N))
   //   SEL[TOK][k]   the selected experts            (int32)
   //   CH [TOK][N]   slot + 1 of a selected expert   (bytes, 0 = not selected)
-  const int LS = N + 1;
+  const int LS = logit_stride(N);
   float* L = reinterpret_cast<float*>(base_ptr);
   int32_t* SEL = reinterpret_cast<int32_t*>(base_ptr + (size_t)TOK * LS * 4);
   uint8_t* CH = base_ptr + (size_t)TOK * LS * 4 + (size_t)TOK * k * 4;
-  bool acc_ok = true;
   if (warp >= 2 && warp < 6) {  // ------------------------------- accumulator -> smem
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;
@@ -204,7 +211,6 @@ route_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
         *abort_flag = 1;
       }
     }
-    acc_ok = ok;
   }
   tc_fence_before();
   __syncthreads();
@@ -214,72 +220,86 @@ route_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
                  "r"(f.tmem_cols)
                  : "memory");
   }
-  // ---------------------------------------------------- per-token decisions (4 warps)
+  // ------------------------------------------- per-token decisions (all 8 warps)
+  // Two threads per token, adjacent lanes: thread h of token r takes the experts of
+  // parity h. Every thread runs the max, the sum and the picks (so the pair's shuffles
+  // are never divergent); only live tokens write. Any timeout (abort flag) leaves every
+  // token of the tile without a decision, as padding.
   const bool masked = a.valid != nullptr;
   const bool want_d2 = a.aux_std2 != nullptr;
   float d2 = 0.f;
-  if (warp >= 2 && warp < 6) {
-    const int r = (warp & 3) * 32 + lane;
+  {
+    const unsigned FULL = 0xffffffffu;
+    const int r = threadIdx.x >> 1, h = threadIdx.x & 1;
     const int t = m0 + r;
     float* row = L + r * LS;
     uint8_t* ch = CH + (size_t)r * N;
-    for (int e = 0; e < N; ++e) ch[e] = 0;
-    const bool live = acc_ok && t < a.T && (!masked || a.valid[t] != 0);
-    s_valid[r] = live ? 1 : 0;
-    if (live) {
-      float m = -INFINITY;
+    int32_t* sel = SEL + r * k;
+    for (int e = h; e < N; e += 2) ch[e] = 0;
+    const bool live = *abort_flag == 0 && t < a.T && (!masked || a.valid[t] != 0);
+    if (h == 0) s_valid[r] = live ? 1 : 0;
+    float m = -INFINITY;
 #pragma unroll 8
-      for (int e = 0; e < N; ++e) m = fmaxf(m, row[e]);
-      float sum = 0.f;
+    for (int e = h; e < N; e += 2) m = fmaxf(m, row[e]);
+    m = fmaxf(m, __shfl_xor_sync(FULL, m, 1));
+    float sum = 0.f;
 #pragma unroll 8
-      for (int e = 0; e < N; ++e) sum += expf(row[e] - m);
-      const float inv = 1.f / sum;
-      // top k: pick j is the best logit strictly after pick j-1 in (logit desc, id asc)
-      float pl = INFINITY, l0 = 0.f, zs = 0.f;
-      int pi = -1;
-      for (int j = 0; j < k; ++j) {
-        float bv = -INFINITY;
-        int bi = -1;
+    for (int e = h; e < N; e += 2) sum += expf(row[e] - m);
+    sum += __shfl_xor_sync(FULL, sum, 1);  // the same sum on both threads
+    const float inv = 1.f / sum;
+    // top k: pick j is the best logit strictly after pick j-1 in (logit desc, id asc);
+    // each thread scans its parity, and the pair keeps the better of its two candidates
+    float pl = INFINITY, l0 = 0.f, zs = 0.f;
+    int pi = -1;
+    for (int j = 0; j < k; ++j) {
+      float bv = -INFINITY;
+      int bi = -1;
 #pragma unroll 8
-        for (int e = 0; e < N; ++e) {
-          const float v = row[e];
-          const bool after = v < pl || (v == pl && e > pi);
-          if (after && (bi < 0 || v > bv)) {
-            bv = v;
-            bi = e;
-          }
+      for (int e = h; e < N; e += 2) {
+        const float v = row[e];
+        const bool after = v < pl || (v == pl && e > pi);
+        if (after && (bi < 0 || v > bv)) {
+          bv = v;
+          bi = e;
         }
-        if (bi < 0) {  // only NaN logits leave no candidate: keep the index in range
-          bi = j;
-          bv = row[j];
-        }
-        SEL[r * k + j] = bi;
-        if (j == 0) l0 = bv;
-        zs += expf(bv - l0);
-        pl = bv;
-        pi = bi;
       }
-      for (int j = 0; j < k; ++j) {  // gate weights: softmax over the k selected logits
-        const int e = SEL[r * k + j];
+      const float ov = __shfl_xor_sync(FULL, bv, 1);
+      const int oi = __shfl_xor_sync(FULL, bi, 1);
+      if (oi >= 0 && (bi < 0 || ov > bv || (ov == bv && oi < bi))) {
+        bv = ov;
+        bi = oi;
+      }
+      if (bi < 0) {  // only NaN logits leave no candidate: keep the index in range
+        bi = j;
+        bv = row[j];
+      }
+      if ((j & 1) == h) sel[j] = bi;
+      if (j == 0) l0 = bv;
+      zs += expf(bv - l0);
+      pl = bv;
+      pi = bi;
+    }
+    __syncwarp();  // the pair's picks and zeroed marks are in place
+    if (live) {
+      for (int j = h; j < k; j += 2) {  // gate weights: softmax over the k selected logits
+        const int e = sel[j];
         a.idx[(size_t)t * k + j] = e;
         a.w[(size_t)t * k + j] = expf(row[e] - l0) / zs;
         ch[e] = (uint8_t)(j + 1);
       }
-      const float invN = 1.f / (float)N;
+    } else if (t < a.T) {  // padding: no expert, weight 0
+      for (int j = h; j < k; j += 2) {
+        a.idx[(size_t)t * k + j] = -1;
+        a.w[(size_t)t * k + j] = 0.f;
+      }
+    }
+    __syncwarp();  // the gates have read the logits they need
+    const float invN = 1.f / (float)N;
 #pragma unroll 8
-      for (int e = 0; e < N; ++e) {  // the token's probabilities replace its logits
-        const float pe = expf(row[e] - m) * inv;
-        row[e] = pe;
-        if (want_d2) d2 = fmaf(pe - invN, pe - invN, d2);
-      }
-    } else {
-      for (int e = 0; e < N; ++e) row[e] = 0.f;
-      if (t < a.T) {  // padding: no expert, weight 0
-        for (int j = 0; j < k; ++j) {
-          a.idx[(size_t)t * k + j] = -1;
-          a.w[(size_t)t * k + j] = 0.f;
-        }
-      }
+    for (int e = h; e < N; e += 2) {  // the token's probabilities replace its logits
+      const float pe = live ? expf(row[e] - m) * inv : 0.f;
+      row[e] = pe;
+      if (want_d2 && live) d2 = fmaf(pe - invN, pe - invN, d2);
     }
   }
   __syncthreads();
@@ -385,7 +405,7 @@ cudaError_t launch_route_fused(const SelectArgs& s, const void* x, const void* w
   size_t optin = 0;
   e = smem_optin_bytes(&optin);
   if (e != cudaSuccess) return e;
-  const size_t epi = (size_t)TOK * (s.N + 1) * 4 + (size_t)TOK * s.k * 4 + (size_t)TOK * s.N;
+  const size_t epi = (size_t)TOK * logit_stride(s.N) * 4 + (size_t)TOK * s.k * 4 + (size_t)TOK * s.N;
   const size_t tail = 8 * (2 * MAX_STAGES + 1) + 16;  // barriers, TMEM address, abort flag
   if (optin < static_smem + 1024 + tail) return cudaErrorInvalidValue;
   const size_t avail = optin - static_smem - 1024 - tail;
