@@ -157,7 +157,8 @@ int moe_forward_timed(const moe_cfg* cfg, const void* x, const void* w_router,
 /*
  * Synchronise `stream`, read and clear the workspace status word. Returns MOE_OK,
  * MOE_EDEVICE (a kernel reported a failure; *bits, if not NULL, gets the word) or
- * MOE_ECUDA. Bits: 1 a bounded wait gave up, 2 an index out of range.
+ * MOE_ECUDA. Bits: 1 a bounded wait gave up, 2 an index out of range, 4 a kernel's
+ * shared-memory layout did not fit its allocation (the kernel did no work).
  */
 int moe_get_status(void* workspace, size_t workspace_bytes, void* stream,
                    uint32_t* bits);

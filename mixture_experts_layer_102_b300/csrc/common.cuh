@@ -14,6 +14,7 @@ namespace moe {
 enum : uint32_t {
   STATUS_WAIT_TIMEOUT = 1u,  // a bounded mbarrier wait gave up
   STATUS_BAD_INDEX = 2u,     // an expert index or row outside its range
+  STATUS_BAD_LAYOUT = 4u,    // a kernel's shared-memory carve did not fit its allocation
 };
 
 __device__ __forceinline__ void report(uint32_t* status, uint32_t bits) {

@@ -55,15 +55,27 @@ constexpr int GROUP_M = 8;                            // row tiles per raster ba
 constexpr int EPI_WARPS = 8;
 constexpr int NUM_THREADS = 64 + 32 * EPI_WARPS;
 
+// Shared memory of one CTA, all of it dynamic (the kernel declares no static shared
+// memory): from a 1024-byte-aligned base, the stages, then 256 bytes of barriers, the
+// TMEM address and the abort flag, then the expert layout tables (first row tile and
+// first row of every expert). The allocation adds an allowance for aligning the base;
+// the first KB of a CTA's shared memory is reserved, so the dynamic part normally
+// starts aligned and the allowance goes unused (the kernel checks it).
+constexpr size_t SMEM_OPTIN_MAX = 232448;                     // per-block opt-in limit
 template <int CG>
 struct Shape {
   static constexpr int TILE_M = 128 * CG;                        // rows per work item
   static constexpr int B_BOXES = 3 - CG;                         // B boxes per CTA stage
   static constexpr uint32_t STAGE_BYTES = BOX_BYTES * (1 + B_BOXES);  // 48 KB or 32 KB
-  static constexpr int STAGES = CG == 1 ? 4 : 6;
-  static constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE_BYTES + 256;
+  static constexpr int STAGES = CG == 1 ? 4 : 7;
   static constexpr int BAR_BYTES = 8 * (2 * STAGES + 2 * NUM_ACC + 1) + 8;
   static_assert(BAR_BYTES <= 256, "barrier area");
+  static constexpr size_t TABLE_OFFSET = (size_t)STAGES * STAGE_BYTES + 256;
+  static constexpr size_t CARVE_BYTES = TABLE_OFFSET + 2 * (MAX_EXPERTS + 1) * 4;
+  static constexpr size_t PAD_BYTES =
+      SMEM_OPTIN_MAX - CARVE_BYTES < 1024 ? SMEM_OPTIN_MAX - CARVE_BYTES : 1024;
+  static constexpr size_t SMEM_BYTES = CARVE_BYTES + PAD_BYTES;
+  static_assert(CARVE_BYTES <= SMEM_OPTIN_MAX, "shared memory");
 };
 
 // Instruction descriptor of kind::f16: D fp32 (bits 4-5 = 1), A bf16 (bits 7-9 = 1),
@@ -136,6 +148,10 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
   // the pair MMA relies on: its descriptors address both CTAs' tiles at once.
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
+  if (base - raw > S::PAD_BYTES) {  // the carve would pass the allocation: refuse
+    if (threadIdx.x == 0) report(a.status, STATUS_BAD_LAYOUT);
+    return;
+  }
   uint8_t* base_ptr = smem_raw + (base - raw);
   const uint32_t full_bar = base + S::STAGES * S::STAGE_BYTES;  // [STAGES] (first CTA's used)
   const uint32_t empty_bar = full_bar + 8 * S::STAGES;           // [STAGES]
@@ -184,7 +200,8 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
   // The expert layout comes from the routing kernels, which ran two or more launches
   // before this one and have completed; only the A rows (the previous kernel's output)
   // need the wait below.
-  __shared__ int32_t tfirst[MAX_EXPERTS + 1], roff[MAX_EXPERTS + 1];
+  int32_t* tfirst = reinterpret_cast<int32_t*>(base_ptr + S::TABLE_OFFSET);  // [N+1]
+  int32_t* roff = tfirst + (MAX_EXPERTS + 1);                                  // [N+1]
   for (int i = threadIdx.x; i <= a.N; i += blockDim.x) {
     tfirst[i] = a.tile_first[i];
     roff[i] = a.offsets[i];
