@@ -20,7 +20,7 @@
 //           N=256 K=16; each CTA stages its own 128 A rows and one 128-row half of B
 //           (the W1 box in the first CTA, the W3 box in the second), both CTAs' loads
 //           complete on the first CTA's full barrier, and the first CTA issues the
-//           pair's MMAs and commits them to both CTAs' barriers: 6 stages of 32 KB,
+//           pair's MMAs and commits them to both CTAs' barriers: 7 stages of 32 KB,
 //           a third less shared-memory traffic per SM for the same MMA work.
 // Small expert groups favour CG = 1 (less row padding, more tiles to spread over the
 // SMs); large ones favour CG = 2.
