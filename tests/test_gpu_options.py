@@ -166,6 +166,10 @@ def check_opts(cfg, n_shared=0, activation="swiglu", seq_len=None, token_sample=
 CASES = [
     (MoEConfig("bf16_fused_n256_k8_t4000", 4000, 128, 256, 8, 64, 1.5, "bf16", seed=38), 0,
      "swiglu", None),
+    (MoEConfig("bf16_fused_n16_t6000", 6000, 128, 16, 2, 64, 1.25, "bf16", seed=49), 0,
+     "swiglu", None),
+    (MoEConfig("bf16_fused_n48_k3_t7001_masked_shared", 7001, 64, 48, 3, 64, 1.0, "bf16",
+               seed=50, zipf_bias=True), 1, "swiglu", 500),
     (MoEConfig("bf16_fused_n1_k1_t4096", 4096, 128, 1, 1, 64, None, "bf16", seed=39), 0,
      "swiglu", None),
     (MoEConfig("bf16_fused_k32_n64_masked_shared", 4100, 64, 64, 32, 64, 0.9, "bf16", seed=40,
@@ -371,6 +375,9 @@ REROUTE_CASES = [
      0, "swiglu", None),
     # 256-row tiles on CTA pairs
     (MoEConfig("bf16_reroute_pair", 4096, 128, 4, 2, 128, 1.02, "bf16", seed=44,
+               zipf_bias=True), 0, "swiglu", None),
+    # after the fused routing kernel, with a ragged last tile
+    (MoEConfig("bf16_reroute_fused_t5000", 5000, 128, 24, 2, 64, 0.95, "bf16", seed=51,
                zipf_bias=True), 0, "swiglu", None),
     (MoEConfig("bf16_reroute_masked_shared2_gelu", 1500, 256, 16, 2, 256, 1.0, "bf16", seed=48,
                zipf_bias=True), 2, "gelu", 100),
