@@ -49,16 +49,18 @@ STAGES = ["router_logits", "route_select", "dispatch", "gemm1_swiglu", "gemm2", 
 
 
 def stage_names(cfg) -> list:
-    """The reported stages: bf16 layers of at least 32 tiles of 128 tokens run the
-    router GEMM and the routing decisions as one kernel ("route"); other layers run
-    them as two."""
-    fused = cfg.dtype == "bf16" and (cfg.T + 127) // 128 >= 32
+    """The reported stages, from the library's plan: a layer whose router GEMM and
+    routing decisions run as one kernel reports them as one stage ("route"); other
+    layers report them as two."""
+    from mixture_experts_layer_102_b300 import moe
+    fused = moe.describe(moe.cfg_from(cfg))["fused_routing"]
     return ["route"] + STAGES[2:] if fused else list(STAGES)
 
 
-# launches of this library's kernels per forward (T > 0): one per reported stage
 def launches_per_forward(cfg) -> int:
-    return len(stage_names(cfg))
+    """This library's kernel launches per forward (T > 0), from its plan."""
+    from mixture_experts_layer_102_b300 import moe
+    return moe.describe(moe.cfg_from(cfg))["launches"]
 
 
 def parse_args(argv=None):
@@ -486,6 +488,7 @@ def run_gpu_arm(args, cfg):
         "staged_ms_per_step": round(float(stage_ms.sum(axis=1).mean()), 5),
         "roofline": roofline,
         "gpu_launches": launches_per_forward(cfg) * args.steps,
+        "plan": moe.describe(c, has_bias=dev.router_bias is not None),
         "clocks": clocks,
         "wall_s_timed_region": round(wall, 3),
         "e2e": e2e,

@@ -270,6 +270,29 @@ int moe_forward_ex(const moe_cfg* cfg, const moe_options* opts, const void* x,
                    int32_t* expert_counts, int32_t* kept_counts, void* workspace,
                    size_t workspace_bytes, void* stream, void* const* stage_events);
 
+/*
+ * How moe_forward / moe_forward_ex runs a layer: the plan the host derives from cfg
+ * and opts alone (no CUDA call, no device needed). It is the plan those calls use,
+ * so a caller can report or test it. The expert GEMMs' tile shape depends on whether
+ * a router bias will be passed (has_bias, 0 or 1).
+ */
+typedef struct {
+  int32_t fused_routing;   /* 1: the router GEMM and the routing decisions run as one
+                              kernel (bf16 with at least 32 tiles of 128 tokens) */
+  int32_t routing_block;   /* tokens per routing block (the unit of the per-block
+                              counts that dispatch reads) */
+  int32_t router_ksplit;   /* slices of H the router GEMM splits into (1 when fused) */
+  int32_t gemm1_tile_rows; /* rows per GEMM1 work item: 256 on CTA pairs, else 128 */
+  int32_t gemm2_tile_rows; /* the same for GEMM2 */
+  int32_t launches;        /* kernel launches of one forward with T > 0 (T = 0: none) */
+  int64_t capacity;        /* C without a valid-token mask; -1 for no limit */
+  int64_t workspace_bytes; /* moe_workspace_size_ex(cfg, opts) */
+} moe_plan;
+
+/* Fill *plan for cfg and opts (NULL opts: the base layer). Returns MOE_OK,
+ * MOE_EINVAL (NULL cfg or plan, invalid cfg or options) or MOE_EUNSUPPORTED. */
+int moe_describe(const moe_cfg* cfg, const moe_options* opts, int has_bias, moe_plan* plan);
+
 /* Static description of a status code. */
 const char* moe_strerror(int status);
 

@@ -539,6 +539,31 @@ size_t moe_workspace_size_ex(const moe_cfg* cfg, const moe_options* opts) {
   return make_plan(cfg, op).total;
 }
 
+int moe_describe(const moe_cfg* cfg, const moe_options* opts, int has_bias, moe_plan* plan) {
+  if (plan == nullptr) return MOE_EINVAL;
+  int rc = check_cfg(cfg);
+  if (rc != MOE_OK) return rc;
+  Opts op;
+  rc = read_opts(opts, &op);
+  if (rc != MOE_OK) return rc;
+  rc = check_opts(cfg, op);
+  if (rc != MOE_OK) return rc;
+  Plan p = make_plan(cfg, op);
+  choose_tiles(p, has_bias != 0);
+  const bool tc = p.dtype == MOE_BF16;
+  plan->fused_routing = p.fused ? 1 : 0;
+  plan->routing_block = SELECT_WARPS * p.sel_tpw;
+  plan->router_ksplit = p.ksplit;
+  plan->gemm1_tile_rows = tc && p.pair1 ? TILE_ROWS_2 : TILE_ROWS_1;
+  plan->gemm2_tile_rows = tc && p.pair2 ? TILE_ROWS_2 : TILE_ROWS_1;
+  // routing (one kernel fused, else router + decisions), rerouting, dispatch, two
+  // expert GEMMs, combine: the launches run_route and run_experts make
+  plan->launches = (p.fused ? 1 : 2) + (p.reroute ? 1 : 0) + 1 + 2 + 1;
+  plan->capacity = p.C;
+  plan->workspace_bytes = (int64_t)p.total;
+  return MOE_OK;
+}
+
 int moe_capacity(const moe_cfg* cfg, int64_t* capacity) {
   if (capacity == nullptr) return MOE_EINVAL;
   const int rc = check_cfg(cfg);

@@ -38,6 +38,7 @@ _SIGNATURES = {
     "moe_get_status": (ctypes.c_int, [_P, ctypes.c_size_t, _P, ctypes.POINTER(ctypes.c_uint32)]),
     "moe_route_static": (ctypes.c_int, [_P] + [_P] * 9 + [_P]),
     "moe_workspace_size_ex": (ctypes.c_size_t, [_P, _P]),
+    "moe_describe": (ctypes.c_int, [_P, _P, ctypes.c_int, _P]),
     "moe_route_ex": (ctypes.c_int, [_P, _P] + [_P] * 9 + [_P, ctypes.c_size_t, _P]),
     "moe_forward_ex": (ctypes.c_int, [_P, _P] + [_P] * 13 + [_P, ctypes.c_size_t, _P, _P]),
     "moe_strerror": (ctypes.c_char_p, [ctypes.c_int]),
@@ -87,6 +88,13 @@ class Options:
             t = getattr(self, name)
             if t is not None:
                 _check(t, name, (1,), torch.float32)
+
+
+class MoEPlan(ctypes.Structure):
+    _fields_ = [("fused_routing", ctypes.c_int32), ("routing_block", ctypes.c_int32),
+                ("router_ksplit", ctypes.c_int32), ("gemm1_tile_rows", ctypes.c_int32),
+                ("gemm2_tile_rows", ctypes.c_int32), ("launches", ctypes.c_int32),
+                ("capacity", ctypes.c_int64), ("workspace_bytes", ctypes.c_int64)]
 
 
 class MoEError(RuntimeError):
@@ -139,6 +147,17 @@ def workspace_size(cfg: MoECfg, options: Optional[Options] = None) -> int:
     if n == 0:
         raise MoEError("moe_workspace_size", MOE_EINVAL)
     return int(n)
+
+
+def describe(cfg: MoECfg, options: Optional[Options] = None, has_bias: bool = False) -> dict:
+    """moe_describe: the plan moe_forward follows for cfg (host only, no GPU needed)."""
+    plan = MoEPlan()
+    opts = None if options is None else ctypes.byref(options.to_c())
+    rc = library().moe_describe(ctypes.byref(cfg), opts, 1 if has_bias else 0,
+                                ctypes.byref(plan))
+    if rc != MOE_OK:
+        raise MoEError("moe_describe", rc)
+    return {name: getattr(plan, name) for name, _ in MoEPlan._fields_}
 
 
 def capacity(cfg: MoECfg) -> Optional[int]:

@@ -190,3 +190,65 @@ def test_options_binding_checks_without_a_gpu():
         moe.Options(activation="relu").to_c()
     with pytest.raises(ValueError):
         moe.Options(valid_mask=torch.ones(4, dtype=torch.uint8)).check(4)   # CPU tensor
+
+
+def _plan(config, options=None, has_bias=False, **over):
+    cfg = config.with_(**over) if over else config
+    return moe.describe(moe.cfg_from(cfg), options, has_bias)
+
+
+def test_describe_reports_the_plan_of_each_workload():
+    # the bench layer: fused routing on 128-token blocks, GEMM1 on CTA pairs (512 rows
+    # per expert, 256-row tiles compute at most 12% more rows), GEMM2 on single CTAs
+    p = _plan(configs.BF16_T4096)
+    assert (p["fused_routing"], p["routing_block"], p["router_ksplit"]) == (1, 128, 1)
+    assert (p["gemm1_tile_rows"], p["gemm2_tile_rows"]) == (256, 128)
+    assert p["launches"] == 5 and p["capacity"] == 640
+    assert p["workspace_bytes"] == moe.workspace_size(moe.cfg_from(configs.BF16_T4096))
+    # with a router bias GEMM1 keeps the 1024-rows-per-expert rule for pairs
+    assert _plan(configs.BF16_T4096, has_bias=True)["gemm1_tile_rows"] == 128
+    # Mixtral-shaped: 2048 rows per expert, both GEMMs on pairs
+    p = _plan(configs.MIXTRAL_T8192)
+    assert (p["fused_routing"], p["gemm1_tile_rows"], p["gemm2_tile_rows"]) == (1, 256, 256)
+    assert p["capacity"] == 3072
+    # fine-grained with its Zipf bias: 512 rows per expert, single CTAs for both
+    p = _plan(configs.FINEGRAINED_T16384, has_bias=True)
+    assert (p["fused_routing"], p["gemm1_tile_rows"], p["gemm2_tile_rows"]) == (1, 128, 128)
+    assert p["capacity"] == 615
+    # decode: one tile of tokens, so the router splits K and the decisions follow
+    p = _plan(configs.DECODE_T64)
+    assert p["fused_routing"] == 0 and p["router_ksplit"] > 1 and p["launches"] == 6
+    assert p["capacity"] == -1 and (p["gemm1_tile_rows"], p["gemm2_tile_rows"]) == (128, 128)
+    # float32: the SIMT path, never fused
+    p = _plan(configs.TINY_F32)
+    assert p["fused_routing"] == 0 and p["launches"] == 6
+
+
+def test_describe_fused_threshold_and_options():
+    # fused from 32 tiles of 128 tokens on: T = 3968 is 31 tiles, T = 3969 is 32
+    assert _plan(configs.BF16_T4096, T=3968)["fused_routing"] == 0
+    assert _plan(configs.BF16_T4096, T=3969)["fused_routing"] == 1
+    assert _plan(configs.BF16_T4096, T=3969, dtype="f32")["fused_routing"] == 0
+    # rerouting adds a launch when there is a capacity limit, and nothing without one
+    rr = moe.Options(reroute=True)
+    assert _plan(configs.BF16_T4096, rr)["launches"] == 6
+    assert _plan(configs.BF16_T4096, rr, capacity_factor=None)["launches"] == 5
+    # shared experts count as experts of T rows each in the tile choice and workspace
+    sh = moe.Options(n_shared=2)
+    c = moe.cfg_from(configs.BF16_T4096)
+    assert _plan(configs.BF16_T4096, sh)["workspace_bytes"] == moe.workspace_size(c, sh)
+
+
+def test_describe_rejects_bad_arguments():
+    lib = moe.library()
+    plan = moe.MoEPlan()
+    c = moe.cfg_from(configs.BF16_T4096)
+    assert lib.moe_describe(ctypes.byref(c), None, 0, None) == moe.MOE_EINVAL
+    assert lib.moe_describe(None, None, 0, ctypes.byref(plan)) == moe.MOE_EINVAL
+    bad = moe.make_cfg(T=64, H=128, N=4, k=5, F=64, capacity_factor=None, dtype="bf16")
+    assert lib.moe_describe(ctypes.byref(bad), None, 0, ctypes.byref(plan)) == moe.MOE_EINVAL
+    big = moe.make_cfg(T=64, H=128, N=300, k=2, F=64, capacity_factor=None, dtype="bf16")
+    assert lib.moe_describe(ctypes.byref(big), None, 0, ctypes.byref(plan)) == \
+        moe.MOE_EUNSUPPORTED
+    with pytest.raises(moe.MoEError):
+        moe.describe(c, moe.Options(n_shared=99))

@@ -88,7 +88,8 @@ def test_algorithmic_units_match_hand_counts():
 def test_stage_names_and_launch_counts():
     sys.path.insert(0, ROOT)
     import bench
-    from mixture_experts_layer_102_b300 import configs
+    from mixture_experts_layer_102_b300 import build, configs
+    build.build(quiet=True)  # the stages come from the library's plan (host only)
     bf = configs.BF16_T4096
     f32 = configs.TINY_F32
     assert bench.stage_names(bf) == ["route", "dispatch", "gemm1_swiglu", "gemm2", "combine"]
