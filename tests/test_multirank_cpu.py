@@ -99,3 +99,29 @@ def test_stage_names_and_launch_counts():
     u = bench.algorithmic_units(bf, kept_slots=8192, touched_experts=16)
     assert u["route"][0] == u["router_logits"][0]
     assert u["route"][1] == u["router_logits"][1] + u["route_select"][1]
+
+
+def test_reference_arm_line_has_every_contract_key():
+    # one process (no torchrun environment): rank 0 of 1 prints one JSON line
+    sys.path.insert(0, ROOT)
+    import bench
+    for var in ("RANK", "WORLD_SIZE", "LOCAL_RANK"):
+        os.environ.pop(var, None)
+    buf = io.StringIO()
+    with redirect_stdout(buf):
+        bench.main(["--impl", "reference", "--config", "tiny", "--steps", "2", "--warmup", "1"])
+    lines = [l for l in buf.getvalue().strip().splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+                "cpu_baseline", "e2e"):
+        assert key in d, key
+    assert d["impl"] == "reference" and d["n_gpus"] == 1 and d["value"] > 0
+    assert (d["steps"], d["warmup"]) == (2, 1) and d["higher_is_better"] is True
+    assert d["config"]["workload"] == "tiny_f32_t64_h128_n8_k2_f256"
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1
+    assert cb["unit"] == d["unit"] and cb["sample"]
+    assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}
