@@ -149,3 +149,63 @@ def test_reroute_latest_first_is_caught(monkeypatch):
         return a[::-1].copy(), b[::-1].copy(), c[::-1].copy(), d
     _plant(monkeypatch, "reroute_overflow", reversed_order)
     _fails(pins_opt.test_reroute_hand_example_k1)
+
+
+# ------------------------------------------------------------- layer options
+
+def test_kl_normalised_by_tokens_only_is_caught(monkeypatch):
+    def kl_by_t(idx, N, k):
+        T = idx.shape[0]
+        if T == 0:
+            return 0.0
+        f = om.expert_counts(idx, N) / float(T)  # sums to k, not 1
+        with np.errstate(divide="ignore"):
+            return float(np.sum((1.0 / N) * (np.log(1.0 / N) - np.log(f))))
+    _plant(monkeypatch, "aux_kl_uniform", kl_by_t)
+    _fails(pins_opt.test_kl_is_zero_for_uniform_routing)
+
+
+def test_kl_in_the_reverse_direction_is_caught(monkeypatch):
+    def kl_reversed(idx, N, k):
+        T = idx.shape[0]
+        if T == 0:
+            return 0.0
+        f = om.expert_counts(idx, N) / float(T * k)
+        nz = f > 0
+        return float(np.sum(f[nz] * (np.log(f[nz]) - np.log(1.0 / N))))  # KL(f || uniform)
+    _plant(monkeypatch, "aux_kl_uniform", kl_reversed)
+    _fails(pins_opt.test_kl_two_expert_closed_form)
+
+
+def test_biased_probability_variance_is_caught(monkeypatch):
+    _plant(monkeypatch, "aux_prob_variance",
+           lambda probs: float(np.var(probs)) if probs.size else 0.0)
+    _fails(pins_opt.test_probability_variance_matches_torch_std)
+
+
+def test_tanh_approximation_of_gelu_is_caught(monkeypatch):
+    def gelu_tanh(z):
+        return 0.5 * z * (1.0 + np.tanh(math.sqrt(2.0 / math.pi) * (z + 0.044715 * z ** 3)))
+    _plant(monkeypatch, "gelu", gelu_tanh)
+    _fails(pins_opt.test_gelu_against_torch_and_the_normal_cdf)
+
+
+def test_gelu_expert_with_silu_is_caught(monkeypatch):
+    def silu_expert(x_rows, w1_e, w2_e):
+        xr = np.asarray(x_rows, np.float64)
+        return om.silu(xr @ np.asarray(w1_e, np.float64).T) @ np.asarray(w2_e, np.float64).T
+    _plant(monkeypatch, "gelu_expert", silu_expert)
+    _fails(pins_opt.test_gelu_expert_orientation_and_library)
+
+
+def test_capacity_counting_padding_tokens_is_caught(monkeypatch):
+    # route the whole batch and only then blank the padding rows: padding counts in C
+    def route_all_tokens(x, w_router, bias, k, cf, valid, reroute=False):
+        r = dict(om.route(x, w_router, bias, k, cf, reroute=reroute))
+        pad = ~np.asarray(valid, bool)
+        r["topk_idx"] = np.where(pad[:, None], -1, r["topk_idx"])
+        r["topk_w"] = np.where(pad[:, None], 0.0, r["topk_w"])
+        r["drop_mask"] = np.where(pad[:, None], 1, r["drop_mask"]).astype(np.uint8)
+        return r
+    monkeypatch.setattr(om, "_route_masked", route_all_tokens)
+    _fails(pins_opt.test_capacity_counts_only_valid_tokens)
