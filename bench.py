@@ -199,7 +199,7 @@ class ClockSampler:
 
     def start(self):
         try:
-            self.out = open(os.devnull if False else f"/tmp/moe_clocks_{os.getpid()}.csv", "w")
+            self.out = open(f"/tmp/moe_clocks_{os.getpid()}.csv", "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
                  "--format=csv,noheader,nounits", "-lms", "100"],
@@ -216,13 +216,20 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
         self.out.close()
-        rows = []
         with open(self.out.name) as f:
-            for line in f:
-                parts = [p.strip() for p in line.split(",")]
-                if len(parts) >= 9:
-                    rows.append(parts)
+            lines = f.readlines()
         os.unlink(self.out.name)
+        return self.summarise(lines)
+
+    @staticmethod
+    def summarise(lines):
+        """Median SM clock, the highest maximum clock and every throttle reason seen
+        Active, from the CSV rows of QUERY (noheader, nounits); None without rows."""
+        rows = []
+        for line in lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
         if not rows:
             return None
         sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]

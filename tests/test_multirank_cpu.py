@@ -125,3 +125,44 @@ def test_reference_arm_line_has_every_contract_key():
     assert cb["unit"] == d["unit"] and cb["sample"]
     assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}
+
+
+def test_clock_samples_summary():
+    sys.path.insert(0, ROOT)
+    import bench
+    lines = [
+        "0, 2032, 2032, 812.50, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active\n",
+        "0, 1980, 2032, 1099.10, 0x0000000000000004, Not Active, Not Active, Not Active, Active\n",
+        "0, 2010, 2032, 1002.00, 0x0000000000000004, Not Active, Not Active, Not Active, Active\n",
+        "0, [N/A], [N/A], [N/A], [N/A], [N/A], [N/A], [N/A], [N/A]\n",
+        "\n",
+    ]
+    d = bench.ClockSampler.summarise(lines)
+    assert d == {"sm_mhz": 2010.0, "sm_max_mhz": 2032.0, "reasons": ["sw_power_cap"],
+                 "samples": 4}
+    hot = bench.ClockSampler.summarise(
+        ["0, 1500, 2032, 1100, 0x48, Active, Active, Not Active, Active\n"])
+    assert hot["reasons"] == ["hw_slowdown", "hw_thermal_slowdown", "sw_power_cap"]
+    assert bench.ClockSampler.summarise([]) is None
+
+
+def test_traffic_record_follows_the_captured_sources(tmp_path, monkeypatch):
+    # a record counts only for its workload and while its sources hash as captured
+    import hashlib
+    sys.path.insert(0, ROOT)
+    import bench
+    (tmp_path / "profiles").mkdir()
+    src = tmp_path / "kernel.cu"
+    src.write_text("__global__ void k() {}\n")
+    rec = {"gemm1_swiglu": {"config": "wl", "bytes_per_launch": 123.0,
+                            "sources": ["kernel.cu"],
+                            "sha256": hashlib.sha256(src.read_bytes()).hexdigest()}}
+    (tmp_path / "profiles" / "traffic.json").write_text(json.dumps(rec))
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.traffic_record("gemm1_swiglu", "wl") == 123.0
+    assert bench.traffic_record("gemm1_swiglu", "other") is None
+    assert bench.traffic_record("gemm2", "wl") is None
+    src.write_text("__global__ void k() { /* changed */ }\n")
+    assert bench.traffic_record("gemm1_swiglu", "wl") is None
+    src.unlink()
+    assert bench.traffic_record("gemm1_swiglu", "wl") is None
