@@ -10,7 +10,7 @@ import numpy as np
 import pytest
 
 import oracle as orc
-from mixture_experts_layer_102_b300 import build, configs, moe
+from mixture_experts_layer_102_b300 import build, configs, inputs, moe
 
 ROOT = Path(__file__).resolve().parents[1]
 
@@ -252,3 +252,20 @@ def test_describe_rejects_bad_arguments():
         moe.MOE_EUNSUPPORTED
     with pytest.raises(moe.MoEError):
         moe.describe(c, moe.Options(n_shared=99))
+
+
+@pytest.mark.parametrize("config,has_bias", [(configs.BF16_T4096, False),
+                                             (configs.MIXTRAL_T8192, False),
+                                             (configs.FINEGRAINED_T16384, True)])
+def test_gemm1_tile_choice_agrees_with_the_padding_of_real_routing(config, has_bias):
+    # the host picks 256-row pair tiles for GEMM1 from a model of the expert counts; on
+    # the seeded workloads the oracle's kept counts must bear the choice out: pairs only
+    # where 256-row tiles compute at most 12% more rows than 128-row tiles
+    inp = inputs.make_inputs(config, with_experts=False)
+    r = orc.route(inp.values("x"), inp.values("w_router"), inp.router_bias, config.k,
+                  config.capacity_factor)
+    kept = r["kept_counts"]
+    rows = {m: int(sum(-(-int(c) // m) * m for c in kept)) for m in (128, 256)}
+    ratio = rows[256] / rows[128]
+    pair = moe.describe(moe.cfg_from(config), has_bias=has_bias)["gemm1_tile_rows"] == 256
+    assert pair == (ratio <= 1.12), (config.name, rows, ratio)
