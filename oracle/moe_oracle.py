@@ -377,20 +377,18 @@ def _route_masked(x, w_router, bias, k, capacity_factor, valid, reroute=False):
     return full
 
 
-def moe_forward(x, w_router, bias, w1, w3, w2, k: int, capacity_factor,
-                token_sample: Optional[np.ndarray] = None, n_shared: int = 0,
-                activation: str = "swiglu", valid_mask=None,
-                reroute: bool = False) -> OracleResult:
-    """The whole layer. Routing and capacity always cover every token (capacity
-    depends on token order); the expert FFN and the combine are evaluated for the
-    tokens in ``token_sample`` (all tokens when None). w1/w3/w2 hold the N routed
-    experts followed by ``n_shared`` shared ones (w3 unused for GELU experts)."""
-    T, H = x.shape
-    N = w_router.shape[1]
-    r = route(x, w_router, bias, k, capacity_factor, valid_mask, reroute)
-    tokens = np.arange(T) if token_sample is None else np.asarray(token_sample, np.int64)
+def experts_combine(x, w1, w3, w2, idx, w, drop, tokens, n_shared: int = 0,
+                    activation: str = "swiglu", valid_mask=None) -> np.ndarray:
+    """Steps 6-7 for the given routing decisions: every kept slot (t, s) of the tokens
+    in ``tokens`` runs expert idx[t,s]'s FFN on x[t], and row i of the result is the
+    sum of those outputs weighted by w[t,s] (dropped slots add nothing), plus the
+    outputs of the ``n_shared`` shared experts (experts N.. of w1/w3/w2, weight 1) for
+    the valid tokens. N is the number of routed experts: w1 holds N + n_shared."""
+    H = x.shape[1]
+    N = w1.shape[0] - n_shared
+    tokens = np.asarray(tokens, np.int64)
     out = np.zeros((len(tokens), H), dtype=np.float64)
-    idx, w, drop = r["topk_idx"], r["topk_w"], r["drop_mask"]
+    k = idx.shape[1]
     # Queue every kept slot of the requested tokens on its expert.
     queue = [([], []) for _ in range(N)]
     for i, t in enumerate(tokens):
@@ -418,5 +416,21 @@ def moe_forward(x, w_router, bias, w1, w3, w2, k: int, capacity_factor,
                 e = N + j
                 out[live] += expert_ffn(xs, w1[e], None if w3 is None else w3[e], w2[e],
                                         activation)
+    return out
+
+
+def moe_forward(x, w_router, bias, w1, w3, w2, k: int, capacity_factor,
+                token_sample: Optional[np.ndarray] = None, n_shared: int = 0,
+                activation: str = "swiglu", valid_mask=None,
+                reroute: bool = False) -> OracleResult:
+    """The whole layer. Routing and capacity always cover every token (capacity
+    depends on token order); the expert FFN and the combine are evaluated for the
+    tokens in ``token_sample`` (all tokens when None). w1/w3/w2 hold the N routed
+    experts followed by ``n_shared`` shared ones (w3 unused for GELU experts)."""
+    T = x.shape[0]
+    r = route(x, w_router, bias, k, capacity_factor, valid_mask, reroute)
+    tokens = np.arange(T) if token_sample is None else np.asarray(token_sample, np.int64)
+    out = experts_combine(x, w1, w3, w2, r["topk_idx"], r["topk_w"], r["drop_mask"], tokens,
+                          n_shared, activation, valid_mask)
     r = {key: val for key, val in r.items() if key in OracleResult.__dataclass_fields__}
     return OracleResult(out=out, tokens=tokens, **r)

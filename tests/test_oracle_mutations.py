@@ -209,3 +209,56 @@ def test_capacity_counting_padding_tokens_is_caught(monkeypatch):
         return r
     monkeypatch.setattr(om, "_route_masked", route_all_tokens)
     _fails(pins_opt.test_capacity_counts_only_valid_tokens)
+
+
+# ------------------------------------------- near ties of the rerouting proposals
+
+def _near_ties_variant(n_extra=1, use_room=True, exclude_own=True):
+    """reroute_near_ties with one step changed: n_extra candidates past the m
+    proposals, the room test, or the exclusion of the token's own experts."""
+    def fn(logits, idx, drop, counts, C, margin=om.NEAR_TIE_MARGIN):
+        out = []
+        if C is None:
+            return np.zeros(0, dtype=np.int64)
+        for t in np.nonzero(drop.any(axis=1))[0]:
+            m = int(drop[t].sum())
+            allowed = (counts < C) if use_room else np.ones(len(counts), bool)
+            allowed = allowed.copy()
+            if exclude_own:
+                allowed[idx[t]] = False
+            cand = np.nonzero(allowed)[0]
+            cand = cand[np.lexsort((cand, -logits[t][cand]))]
+            v = logits[t][cand[:m + n_extra]]
+            if v.size >= 2 and (v[:-1] - v[1:] < margin).any():
+                out.append(t)
+        return np.asarray(out, dtype=np.int64)
+    return fn
+
+
+def test_near_ties_over_m_candidates_only_is_caught(monkeypatch):
+    _plant(monkeypatch, "reroute_near_ties", _near_ties_variant(n_extra=0))
+    _fails(pins_opt.test_reroute_near_tie_listed_when_the_best_two_candidates_are_close)
+
+
+def test_near_ties_over_m_plus_two_candidates_is_caught(monkeypatch):
+    _plant(monkeypatch, "reroute_near_ties", _near_ties_variant(n_extra=2))
+    _fails(pins_opt.test_reroute_near_tie_looks_at_m_plus_one_candidates_only)
+
+
+def test_near_ties_ignoring_room_is_caught(monkeypatch):
+    _plant(monkeypatch, "reroute_near_ties", _near_ties_variant(use_room=False))
+    _fails(pins_opt.test_reroute_near_tie_skips_full_and_own_experts)
+
+
+def test_near_ties_with_the_tokens_own_experts_is_caught(monkeypatch):
+    _plant(monkeypatch, "reroute_near_ties", _near_ties_variant(exclude_own=False))
+    _fails(pins_opt.test_reroute_near_tie_skips_full_and_own_experts)
+
+
+def test_near_ties_variant_with_nothing_changed_passes(monkeypatch):
+    # the planted variants differ from the oracle in one step only
+    _plant(monkeypatch, "reroute_near_ties", _near_ties_variant())
+    pins_opt.test_reroute_near_tie_listed_when_the_best_two_candidates_are_close()
+    pins_opt.test_reroute_near_tie_looks_at_m_plus_one_candidates_only()
+    pins_opt.test_reroute_near_tie_skips_full_and_own_experts()
+    pins_opt.test_reroute_near_ties_are_exactly_the_unstable_proposals()

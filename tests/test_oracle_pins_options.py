@@ -272,3 +272,93 @@ def test_reroute_invariants(cf):
                 assert room_left[allowed[j]] == 0, (t, s, allowed[j])
             elif not drop[t, s]:
                 assert idx[t, s] == allowed[j]
+
+
+# ------------------------------------------- near ties of the rerouting proposals
+
+def _near(logits, idx, drop, counts, C):
+    return orc.reroute_near_ties(np.asarray(logits, np.float64)[None, :],
+                                 np.asarray([idx]), np.asarray([drop], np.uint8),
+                                 np.asarray(counts), C).tolist()
+
+
+def test_reroute_near_tie_listed_when_the_best_two_candidates_are_close():
+    # one dropped slot (m = 1): its proposal is the best expert with room that the
+    # token did not select; experts 3 and 2 (both with room) are 5e-5 apart, so the
+    # proposal may flip between them
+    L = [9, 8, 3.0, 3.00005, 1, 0]
+    assert _near(L, [0, 1], [0, 1], [5, 5, 0, 0, 0, 0], 2) == [0]
+    # 1e-3 apart: the proposal is decided
+    L2 = [9, 8, 3.0, 3.001, 1, 0]
+    assert _near(L2, [0, 1], [0, 1], [5, 5, 0, 0, 0, 0], 2) == []
+
+
+def test_reroute_near_tie_looks_at_m_plus_one_candidates_only():
+    # m = 1: the best candidate (expert 2) is far ahead; the close pair (4, 3) is the
+    # second and third candidate, which cannot change the one proposal
+    L = [9, 8, 5.0, 3.0, 3.00005, 0]
+    assert _near(L, [0, 1], [0, 1], [5, 5, 0, 0, 0, 0], 2) == []
+    # m = 2 (both slots dropped): the second proposal is between 4 and 3
+    assert _near(L, [0, 1], [1, 1], [5, 5, 0, 0, 0, 0], 2) == [0]
+
+
+def test_reroute_near_tie_skips_full_and_own_experts():
+    L = [9, 8, 3.0, 3.00005, 1, 0]
+    # expert 3 is full (count 2 = C): the candidates are 2, 4, 5, far apart
+    assert _near(L, [0, 1], [0, 1], [5, 5, 0, 2, 0, 0], 2) == []
+    # the token's own expert 1 sits next to candidate 2 but is not a candidate
+    L3 = [9, 3.00005, 3.0, 1, 0.5, 0]
+    assert _near(L3, [0, 1], [0, 1], [5, 0, 0, 0, 0, 0], 2) == []
+
+
+def test_reroute_near_tie_empty_without_drops_or_capacity():
+    L = [9, 8, 3.0, 3.00005, 1, 0]
+    assert _near(L, [0, 1], [0, 0], [5, 5, 0, 0, 0, 0], 2) == []
+    assert _near(L, [0, 1], [0, 1], [5, 5, 0, 0, 0, 0], None) == []
+
+
+def _proposals(logits_t, idx_t, counts, C, m):
+    """The m proposals of a token by brute force: every expert with room that the
+    token did not select, ordered by (logit desc, id asc)."""
+    cand = sorted((e for e in range(len(logits_t)) if counts[e] < C and e not in idx_t),
+                  key=lambda e: (-logits_t[e], e))
+    return cand[:m]
+
+
+def test_reroute_near_ties_are_exactly_the_unstable_proposals():
+    # On a Zipf-skewed batch whose logits are rounded to a 1e-4 grid (so that many
+    # candidates tie or sit one grid step apart): a token that is NOT listed keeps its
+    # proposals under every perturbation of its logits by less than half the margin,
+    # and a listed one changes them when the closest pair among its first m+1
+    # candidates moves apart in the other direction by about half the margin each.
+    cfg = configs.TINY_F32.with_(T=400, N=12, k=2, capacity_factor=0.7, zipf_bias=True)
+    inp = inputs.make_inputs(cfg, with_experts=False)
+    base = orc.route(inp.x, inp.w_router, inp.router_bias, 2, 0.7)
+    logits = np.round(base["logits"] * 1e4) / 1e4
+    idx = orc.topk_select(logits, 2)
+    counts = orc.expert_counts(idx, 12)
+    C = base["capacity"]
+    _, drop, _ = orc.capacity_assign(idx, 12, C)
+    listed = set(orc.reroute_near_ties(logits, idx, drop, counts, C).tolist())
+    rng = np.random.default_rng(3)
+    n_listed = n_stable = 0
+    for t in np.nonzero(drop.any(axis=1))[0]:
+        m = int(drop[t].sum())
+        prop = _proposals(logits[t], idx[t].tolist(), counts, C, m)
+        if t in listed:
+            n_listed += 1
+            cand = _proposals(logits[t], idx[t].tolist(), counts, C, m + 1)
+            v = logits[t][cand]
+            j = int(np.argmin(v[:-1] - v[1:]))
+            delta = 0.5 * (v[j] - v[j + 1]) + 1e-7   # < half the margin plus 1e-7
+            assert delta < 0.5e-4 + 1e-7
+            swapped = logits[t].copy()
+            swapped[cand[j]] -= delta
+            swapped[cand[j + 1]] += delta
+            assert _proposals(swapped, idx[t].tolist(), counts, C, m) != prop
+        else:
+            n_stable += 1
+            for _ in range(20):
+                noisy = logits[t] + rng.uniform(-0.49e-4, 0.49e-4, size=12)
+                assert _proposals(noisy, idx[t].tolist(), counts, C, m) == prop
+    assert n_listed > 0 and n_stable > 0
