@@ -8,3 +8,12 @@ if ROOT not in sys.path:
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a B300 (sm_103a) GPU")
+
+
+def pytest_terminal_summary(terminalreporter, exitstatus, config):
+    import parity_report
+    rows = parity_report.lines()
+    if rows:
+        terminalreporter.section("parity figures (GPU vs oracle)")
+        for r in rows:
+            terminalreporter.write_line(r)

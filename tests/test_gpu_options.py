@@ -22,6 +22,7 @@ import pytest
 import torch
 
 import oracle as orc
+import parity_report
 from mixture_experts_layer_102_b300 import configs, inputs, moe
 from mixture_experts_layer_102_b300.configs import MoEConfig
 
@@ -47,6 +48,13 @@ def _rel_err(y, r):
         return 0.0
     rms = np.sqrt(np.mean(r * r))
     return float(np.max(np.abs(y - r) / (np.abs(r) + rms + 1e-30)))
+
+
+def _max_ratio(y, r):
+    """max |y - r| / max |r|, reported beside the gated metric."""
+    if r.size == 0 or not np.abs(r).max() > 0:
+        return 0.0
+    return float(np.abs(y - r).max() / np.abs(r).max())
 
 
 def run_opts(cfg, inp, n_shared=0, activation="swiglu", mask=None, reroute=False):
@@ -147,10 +155,14 @@ def compare_opts(cfg, g, ref, mask, n_shared):
     dropped_all = ref.drop_mask[rows].all(axis=1) & valid[rows]
     live = keep & valid[rows] & (~dropped_all if n_shared == 0 else True)
     err = _rel_err(g["out"][rows[live]], ref.out[live])
+    info = dict(err=err, max_ratio=_max_ratio(g["out"][rows[live]], ref.out[live]),
+                near_tie_set=len(set_ties), near_tie_order=len(order_ties),
+                flipped=len(flipped), reordered=len(reordered), valid=int(valid.sum()))
+    parity_report.record(f"{cfg.name} (S={n_shared})", **info)
     assert err <= TOL[cfg.dtype], f"output relative error {err:.3e} > {TOL[cfg.dtype]}"
     if n_shared == 0:
         assert (g["out"][rows[dropped_all & keep]] == 0).all()
-    return dict(err=err, flipped=len(flipped), valid=int(valid.sum()))
+    return info
 
 
 def check_opts(cfg, n_shared=0, activation="swiglu", seq_len=None, token_sample=None):
@@ -345,11 +357,14 @@ def compare_reroute(cfg, g, ref, mask, n_shared):
     dropped_all = ref.drop_mask[rows].all(axis=1) & vr
     live = vr & (~dropped_all if n_shared == 0 else True)
     err = _rel_err(g["out"][rows[live]], ref.out[live])
+    info = dict(err=err, max_ratio=_max_ratio(g["out"][rows[live]], ref.out[live]),
+                rerouted=int(ref.rerouted.sum()), dropped=int(ref.drop_mask[valid].sum()))
+    parity_report.record(f"{cfg.name} (separated logits, rerouting)", **info)
     assert err <= TOL[cfg.dtype], f"output relative error {err:.3e} > {TOL[cfg.dtype]}"
     assert (g["out"][rows[~vr]] == 0).all()
     if n_shared == 0:
         assert (g["out"][rows[dropped_all]] == 0).all()
-    return dict(err=err, rerouted=int(ref.rerouted.sum()), dropped=int(ref.drop_mask[valid].sum()))
+    return info
 
 
 def check_reroute(cfg, n_shared=0, activation="swiglu", seq_len=None, token_sample=None):
@@ -417,3 +432,146 @@ def test_route_ex_with_reroute_matches_forward_ex():
     assert moe.get_status(ws) == 0
     for name in ("topk_idx", "topk_w", "aux_loss", "drop_mask", "expert_counts", "kept_counts"):
         assert (getattr(r, name).cpu().numpy() == g[name]).all(), name
+
+
+# ------------------------------------- overflow rerouting on ordinary router logits
+#
+# Inputs from the ordinary recipe (inputs.make_inputs): the GPU's fp32 logits differ
+# from the oracle's fp64 ones by accumulation rounding, so near ties may resolve
+# differently. The comparison conditions on the GPU's own routing before rerouting
+# (the same call without the option), as the capacity comparison above does:
+#
+# 1. that routing must match the oracle's, except tokens in its near-tie set (set
+#    flips) or near-tie order set (slot order);
+# 2. a conditional oracle runs capacity and one round of rerouting on it with the
+#    fp64 logits (oracle.capacity_assign, oracle.reroute_overflow);
+# 3. a token whose dropped slots' proposals may flip (oracle.reroute_near_ties) can
+#    change which proposals reach which expert, so the experts in its tied groups
+#    are "affected". Every token that is not tied and proposes no affected expert
+#    must match the conditional oracle exactly; the others must be a valid outcome
+#    (distinct experts, moves only from dropped slots to experts with room that the
+#    token did not select, among its first m+1 candidates, room respected);
+# 4. outputs: the oracle's expert FFNs and combine (oracle.experts_combine) on the
+#    GPU's final routing with the fp64 gate weights of the GPU's first routing.
+
+def _candidates(logits_t, own, counts, C):
+    """Experts a token may move to, best first (brute force)."""
+    return sorted((e for e in range(len(logits_t)) if counts[e] < C and e not in own),
+                  key=lambda e: (-logits_t[e], e))
+
+
+def check_reroute_ordinary(cfg, token_sample=None, want_split=None):
+    inp = inputs.make_inputs(cfg)
+    g, (c, dev, ws, opts) = run_opts(cfg, inp, reroute=True)
+    if want_split is not None:
+        assert (moe.describe(c)["router_ksplit"] > 1) == want_split
+    r0 = moe.route(c, dev.x, dev.w_router, dev.router_bias)   # the routing before rerouting
+    idx0 = r0.topk_idx.cpu().numpy().astype(np.int64)
+    w0 = r0.topk_w.cpu().numpy()
+    drop0_g = r0.drop_mask.cpu().numpy()
+    T, k, N = cfg.T, cfg.k, cfg.N
+    x, wr = inp.values("x"), inp.values("w_router")
+    ref = orc.route(x, wr, inp.router_bias, k, cfg.capacity_factor)
+    L = ref["logits"]
+    C = ref["capacity"]
+
+    # 1. the first routing against the oracle's
+    same_set = (np.sort(idx0, axis=1) == np.sort(ref["topk_idx"], axis=1)).all(axis=1)
+    flipped = np.nonzero(~same_set)[0]
+    assert set(flipped.tolist()) <= set(ref["near_tie_set"].tolist())
+    reordered = np.nonzero(same_set & (idx0 != ref["topk_idx"]).any(axis=1))[0]
+    assert set(reordered.tolist()) <= set(ref["near_tie_order"].tolist())
+    w_ref = orc.gate_weights(L, idx0)
+    assert np.abs(w0 - w_ref).max() <= TOL_W
+    assert abs(float(g["aux_loss"][0]) - ref["aux_loss"]) <= TOL_AUX
+
+    # 2. the conditional oracle on the GPU's first routing
+    counts = orc.expert_counts(idx0, N)
+    _, drop0, _ = orc.capacity_assign(idx0, N, C)
+    assert (drop0_g == drop0).all()
+    assert (g["expert_counts"] == counts).all()           # the original routing's counts
+    idx_c, drop_c, rer_c, acc_c = orc.reroute_overflow(L, idx0, drop0, counts, C)
+    ties = set(orc.reroute_near_ties(L, idx0, drop0, counts, C).tolist())
+
+    # 3. affected experts: the tied groups among each tied token's first m+1
+    #    candidates, each from the first tied token that may propose it (experts
+    #    accept in token order, so earlier proposals are not affected)
+    first_tie = {}
+    props = {}
+    for t in np.nonzero(drop0.any(axis=1))[0]:
+        m = int(drop0[t].sum())
+        cand = _candidates(L[t], set(idx0[t].tolist()), counts, C)
+        props[t] = cand[:m]
+        if t in ties:
+            v = L[t][cand[:m + 1]]
+            for j in range(len(v) - 1):
+                if v[j] - v[j + 1] < orc.NEAR_TIE_MARGIN:
+                    for e in (cand[j], cand[j + 1]):
+                        first_tie.setdefault(e, t)
+    affected = set(first_tie)
+    idx_f, drop_f = g["topk_idx"].astype(np.int64), g["drop_mask"]
+    exact = np.array([t not in ties and all(t < first_tie.get(e, T) for e in props.get(t, []))
+                      for t in range(T)])
+    assert (idx_f[exact] == idx_c[exact]).all(), "final experts differ"
+    assert (drop_f[exact] == drop_c[exact]).all(), "final drops differ"
+    assert (g["topk_w"] == w0).all()                       # moved slots keep their weights
+    moved = idx_f != idx0
+    assert (drop0[moved] == 1).all() and (drop_f[moved] == 0).all()
+    room = np.maximum(C - counts, 0)
+    for t in np.nonzero(~exact)[0]:
+        assert len(set(idx_f[t].tolist())) == k
+        m = int(drop0[t].sum())
+        cand = _candidates(L[t], set(idx0[t].tolist()), counts, C)[:m + 1]
+        for s in np.nonzero(moved[t])[0]:
+            assert idx_f[t, s] in cand
+    final = np.bincount(idx_f[drop_f == 0], minlength=N)
+    assert (g["kept_counts"] == final).all() and (final <= C).all()
+    assert (np.bincount(idx_f[moved], minlength=N) <= room).all()
+
+    # 4. outputs on the GPU's final routing
+    tokens = np.arange(T) if token_sample is None else np.asarray(token_sample)
+    y_ref = orc.experts_combine(x, inp.values("w1"), inp.values("w3"), inp.values("w2"),
+                                idx_f, w_ref, drop_f, tokens)
+    dead = drop_f[tokens].all(axis=1)
+    assert (g["out"][tokens[dead]] == 0).all()
+    err = _rel_err(g["out"][tokens[~dead]], y_ref[~dead])
+    info = dict(err=err, max_ratio=_max_ratio(g["out"][tokens[~dead]], y_ref[~dead]),
+                near_tie_set=len(ref["near_tie_set"]),
+                near_tie_order=len(ref["near_tie_order"]), flipped=len(flipped),
+                reroute_ties=len(ties), affected_experts=len(affected),
+                checked_exactly=int(exact.sum()), rerouted=int(moved.sum()),
+                dropped=int(drop_f.sum()))
+    parity_report.record(f"{cfg.name} (ordinary logits, rerouting)", **info)
+    assert err <= TOL[cfg.dtype], f"output relative error {err:.3e} > {TOL[cfg.dtype]}"
+    assert info["rerouted"] > 0
+    return info
+
+
+REROUTE_ORDINARY = [
+    # the fused routing kernel (>= 32 tiles of 128 tokens), Zipf-skewed experts
+    (MoEConfig("bf16_reroute_real_fused_zipf", 4096, 256, 32, 2, 128, 1.1, "bf16", seed=61,
+               zipf_bias=True), False),
+    # the split-K tensor-core router and the routing-decision kernel
+    (MoEConfig("bf16_reroute_real_splitk", 1500, 512, 16, 2, 256, 0.9, "bf16", seed=62,
+               zipf_bias=True), True),
+    # float32: CUDA-core router
+    (MoEConfig("f32_reroute_real", 300, 192, 16, 2, 320, 1.0, "f32", seed=63, zipf_bias=True),
+     None),
+    # k = 4 with hot and cold experts (a uniform router at CF < 1 would leave no room)
+    (MoEConfig("bf16_reroute_real_k4", 2000, 256, 16, 4, 128, 1.0, "bf16", seed=64,
+               zipf_bias=True), None),
+]
+
+
+@pytest.mark.parametrize("case", REROUTE_ORDINARY, ids=lambda c: c[0].name)
+def test_reroute_on_ordinary_logits(case):
+    cfg, split = case
+    check_reroute_ordinary(cfg, want_split=split)
+
+
+def test_reroute_on_the_finegrained_workload_sampled():
+    # the fine-grained Zipf-skewed workload itself: routing for every token, outputs on
+    # a seeded sample of rows
+    cfg = configs.FINEGRAINED_T16384
+    sample = np.sort(np.random.default_rng(11).choice(cfg.T, size=256, replace=False))
+    check_reroute_ordinary(cfg, token_sample=sample)

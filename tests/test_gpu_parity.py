@@ -22,6 +22,7 @@ import pytest
 import torch
 
 import oracle as orc
+import parity_report
 from mixture_experts_layer_102_b300 import configs, inputs, moe
 from mixture_experts_layer_102_b300.configs import MoEConfig
 
@@ -55,6 +56,13 @@ def _rel_err(y, r):
     if r.size == 0:
         return 0.0
     return float(np.max(np.abs(y - r) / (np.abs(r) + rms + 1e-30)))
+
+
+def _max_ratio(y, r):
+    """max |y - r| / max |r|, reported beside the gated metric."""
+    if r.size == 0 or not np.abs(r).max() > 0:
+        return 0.0
+    return float(np.abs(y - r).max() / np.abs(r).max())
 
 
 def run_gpu(cfg: MoEConfig, inp):
@@ -137,10 +145,14 @@ def compare(cfg: MoEConfig, g, ref):
     y = g["out"][rows[live]]
     r = ref.out[live]
     err = _rel_err(y, r)
+    info = dict(err=err, max_ratio=_max_ratio(y, r), near_tie_set=len(set_ties),
+                near_tie_order=len(order_ties), flipped=len(flipped),
+                reordered=len(reordered), drops=int(ref.drop_mask.sum()),
+                rows=int(keep.sum()))
+    parity_report.record(cfg.name, **info)
     assert err <= TOL[cfg.dtype], f"output relative error {err:.3e} > {TOL[cfg.dtype]}"
     assert (g["out"][rows[dropped_all & keep]] == 0).all()
-    return dict(err=err, flipped=len(flipped), near_ties=len(set_ties),
-                drops=int(ref.drop_mask.sum()), rows=int(keep.sum()))
+    return info
 
 
 # ------------------------------------------------------------------ small cases
