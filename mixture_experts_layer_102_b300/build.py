@@ -84,12 +84,42 @@ def build(force: bool = False, ptxas_verbose: bool = False, quiet: bool = False)
     return LIB_PATH
 
 
+HOOKS_LIB_PATH = os.path.join(HERE, "libmoe_b300_testhooks.so")
+
+
+def build_test_hooks(force: bool = False, quiet: bool = False) -> str:
+    """The test build of the library (include/moe_test_hooks.h): the product objects
+    with gemm_tc.cu recompiled under MOE_TEST_HOOKS, linked as
+    ``libmoe_b300_testhooks.so``. Only tests load it."""
+    build(force=force, quiet=quiet)
+    deps = _deps() + [os.path.join(INCLUDE, "moe_test_hooks.h")]
+    if (not force and os.path.exists(HOOKS_LIB_PATH)
+            and all(os.path.getmtime(f) <= os.path.getmtime(HOOKS_LIB_PATH) for f in deps)):
+        return HOOKS_LIB_PATH
+    nvcc = _nvcc()
+    obj = os.path.join(BUILD_DIR, "gemm_tc_hooks.o")
+    cmd = [nvcc, "-c", os.path.join(CSRC, "gemm_tc.cu"), "-o", obj, "-DMOE_TEST_HOOKS"] + ARCH + \
+        ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError("nvcc failed on gemm_tc.cu (test hooks):\n" + r.stdout + r.stderr)
+    objs = [os.path.join(BUILD_DIR, s.replace(".cu", ".o")) for s in SOURCES if s != "gemm_tc.cu"]
+    tmp = HOOKS_LIB_PATH + ".tmp"
+    r = subprocess.run([nvcc, "-shared"] + ARCH + ["-o", tmp] + objs + [obj],
+                       capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError("link failed:\n" + r.stdout + r.stderr)
+    os.replace(tmp, HOOKS_LIB_PATH)
+    return HOOKS_LIB_PATH
+
+
 def main() -> None:
     ap = argparse.ArgumentParser()
     ap.add_argument("--force", action="store_true")
     ap.add_argument("--ptxas-verbose", action="store_true")
     args = ap.parse_args()
     print(build(force=args.force, ptxas_verbose=args.ptxas_verbose))
+    print(build_test_hooks())
 
 
 if __name__ == "__main__":

@@ -51,7 +51,7 @@ constexpr uint32_t BOX_BYTES = 128 * BK * 2;          // one 128-row x 64 box: 1
 constexpr int ACC_COLS = 256;
 constexpr int NUM_ACC = 2;
 constexpr uint32_t TMEM_COLS = 512;
-constexpr int GROUP_M = 8;                            // row tiles per raster band
+constexpr int GROUP_MAX = 16;                         // most row tiles per raster band
 constexpr int EPI_WARPS = 8;
 constexpr int NUM_THREADS = 64 + 32 * EPI_WARPS;
 
@@ -99,9 +99,12 @@ __device__ __forceinline__ float gelu_erf(float z) {
 
 // Work item w -> (expert, row tile, column tile). Items are grouped by expert (an
 // expert's tiles x all column tiles, experts in order); inside an expert, bands of
-// GROUP_M row tiles sweep the column tiles with the row tile fastest, so the units in
-// flight share a few A tiles and each weight tile of the expert is streamed about once
-// per band. `tfirst` [N+1] holds each expert's first row tile (shared memory).
+// row tiles sweep the column tiles with the row tile fastest, so the units in flight
+// share a few A tiles and each weight tile of the expert is streamed about once per
+// band. An expert of `tiles` row tiles gets ceil(tiles / GROUP_MAX) bands whose
+// heights differ by at most one: a lone short band at the end would stream the
+// expert's whole weight set once more for a few rows. `tfirst` [N+1] holds each
+// expert's first row tile (shared memory).
 __device__ __forceinline__ void raster(int w, const int32_t* tfirst, int N, int n_tiles, int& e,
                                        int& mt, int& nt) {
   int lo = 0, hi = N - 1;  // last expert whose first item is <= w
@@ -110,13 +113,15 @@ __device__ __forceinline__ void raster(int w, const int32_t* tfirst, int N, int 
     if (tfirst[mid] * n_tiles <= w) lo = mid; else hi = mid - 1;
   }
   const int t0 = tfirst[lo];
-  const int tiles = tfirst[lo + 1] - t0;
+  const int tiles = tfirst[lo + 1] - t0;  // >= 1: w lies in this expert's items
   const int local = w - t0 * n_tiles;
-  const int band_size = GROUP_M * n_tiles;
-  const int band = local / band_size;
-  const int in_band = local - band * band_size;
-  const int m_first = band * GROUP_M;
-  const int gm = min(GROUP_M, tiles - m_first);
+  const int nb = (tiles + GROUP_MAX - 1) / GROUP_MAX;
+  const int base = tiles / nb, rem = tiles - base * nb;  // rem bands of base + 1 rows
+  const int r = local / n_tiles;  // the band holding item `local` holds row tile r
+  const int band = r < rem * (base + 1) ? r / (base + 1) : rem + (r - rem * (base + 1)) / base;
+  const int m_first = band * base + min(band, rem);
+  const int gm = base + (band < rem ? 1 : 0);
+  const int in_band = local - m_first * n_tiles;
   mt = t0 + m_first + in_band % gm;
   nt = in_band / gm;
   e = lo;
@@ -135,6 +140,9 @@ struct TcArgs {
   int n_valid;       // output columns in total
   int b1_row_off;    // row offset of the second CTA's B box: 0 (W3) or 128 (W2)
   uint32_t* status;
+#ifdef MOE_TEST_HOOKS
+  int test_skip_kchunk;  // k-chunk of CTA 0's first item whose loads are withheld, -1: none
+#endif
 };
 
 template <int EPI, int CG>
@@ -238,12 +246,22 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
       // The weights are the caller's: the first unit's weight boxes for the first
       // STAGES k-chunks go out before the wait for the previous kernel (the stages are
       // fresh, so no empty-barrier wait is due), and only their A boxes follow it.
+#ifdef MOE_TEST_HOOKS
+      // Test builds only: on single-CTA tiles, CTA 0 issues no load (and no expected
+      // byte count) for one k-chunk of its first work item. That stage's full barrier
+      // then never completes, the MMA thread's bounded wait gives up, and the abort
+      // path runs: nothing is in flight for the withheld stage.
+      const int skip_kc = (CG == 1 && blockIdx.x == 0) ? a.test_skip_kchunk : -1;
+#else
+      constexpr int skip_kc = -1;
+#endif
       int pre = 0;
       if (unit < total) {
         int e, mt, nt;
         raster(unit, tfirst, a.N, a.n_tiles, e, mt, nt);
         pre = min(S::STAGES, kchunks);
         for (int kc = 0; kc < pre; ++kc) {
+          if (kc == skip_kc) continue;
           if (leader) mbar_expect_tx(full_bar + 8 * kc, CG * S::STAGE_BYTES);
           load_b(base + kc * S::STAGE_BYTES, full_c + 8 * kc, kc, nt * a.n_per_tile, e);
         }
@@ -262,17 +280,19 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
         for (int kc = 0; kc < kchunks; ++kc, ++issued) {
           const uint32_t sA = base + stage * S::STAGE_BYTES;
           const uint32_t fb = full_c + 8 * stage;
-          if (issued >= pre) {
-            if (!mbar_wait(empty_bar + 8 * stage, phase ^ 1u, abort_flag, WAIT_LIMIT_NS)) {
-              ok = false;
-              break;
+          if (!(w == unit && kc == skip_kc)) {
+            if (issued >= pre) {
+              if (!mbar_wait(empty_bar + 8 * stage, phase ^ 1u, abort_flag, WAIT_LIMIT_NS)) {
+                ok = false;
+                break;
+              }
+              if (leader) mbar_expect_tx(full_bar + 8 * stage, CG * S::STAGE_BYTES);
+              load_b(sA, fb, kc, n0, e);
             }
-            if (leader) mbar_expect_tx(full_bar + 8 * stage, CG * S::STAGE_BYTES);
-            load_b(sA, fb, kc, n0, e);
+            tma_load_2d<CG>(sA, &tmA, fb, kc * BK, row0);
+            used |= 1u << stage;
+            last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
           }
-          tma_load_2d<CG>(sA, &tmA, fb, kc * BK, row0);
-          used |= 1u << stage;
-          last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
           if (++stage == S::STAGES) {
             stage = 0;
             phase ^= 1u;
@@ -438,6 +458,10 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
 
 // ------------------------------------------------------------------ host side
 
+#ifdef MOE_TEST_HOOKS
+int g_test_skip_kchunk = -1;  // see moe_test_withhold_gemm_load
+#endif
+
 // Work units (CTAs, or CTA pairs) that can be resident at once: the grid size.
 template <int EPI, int CG>
 int grid_units() {
@@ -529,6 +553,9 @@ cudaError_t launch_grouped_gemm_tc(const GroupedGemmArgs& a, cudaStream_t stream
   t.n_valid = a.n_cols;
   t.b1_row_off = swiglu ? 0 : 128;
   t.status = a.status;
+#ifdef MOE_TEST_HOOKS
+  t.test_skip_kchunk = g_test_skip_kchunk;
+#endif
   switch (a.epi) {
     case EPI_SWIGLU:
       return a.pair ? launch_t<EPI_SWIGLU, 2>(mA, mB0, mB1, t, stream, pdl)
@@ -543,3 +570,7 @@ cudaError_t launch_grouped_gemm_tc(const GroupedGemmArgs& a, cudaStream_t stream
 }
 
 }  // namespace moe
+
+#ifdef MOE_TEST_HOOKS
+extern "C" void moe_test_withhold_gemm_load(int kchunk) { moe::g_test_skip_kchunk = kchunk; }
+#endif
