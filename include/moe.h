@@ -176,11 +176,13 @@ int moe_get_status(void* workspace, size_t workspace_bytes, void* stream,
  * The call allocates nothing. It returns MOE_EUNSUPPORTED when the layer's routing
  * scratch does not fit that array (roughly: ksplit*T*N*4 partial logits plus about
  * 16*T*k bytes; every named workload here fits). The first call on a device looks
- * up the array's device address (cudaGetSymbolAddress) with that device current;
- * make that first call before any stream capture. All calls share the array and it
- * keeps the last call's contents: calls that overlap on the GPU (other streams,
- * other threads) race and must be serialised by the caller. Device-side status bits
- * are cleared at the start of each call and are not reported.
+ * up the array's device address (cudaGetSymbolAddress) with that device current and
+ * keeps it for the life of the process; make that first call before any stream
+ * capture, and do not use this call on a device after cudaDeviceReset() on it (the
+ * kept address would be stale). All calls share the array and it keeps the last
+ * call's contents: calls that overlap on the GPU (other streams, other threads) race
+ * and must be serialised by the caller. Each call clears the array's status word
+ * before its kernels run; moe_get_status_static() reads what they reported.
  */
 #define MOE_STATIC_SCRATCH_BYTES ((size_t)16 << 20)
 
@@ -188,6 +190,14 @@ int moe_route_static(const moe_cfg* cfg, const void* x, const void* w_router,
                      const float* router_bias, int32_t* topk_idx, float* topk_w,
                      float* aux_loss, uint8_t* drop_mask, int32_t* expert_counts,
                      int32_t* kept_counts, void* stream);
+
+/*
+ * moe_get_status for moe_route_static: synchronise `stream`, then read and clear the
+ * status word of the static scratch array on the current device. Returns MOE_OK,
+ * MOE_EDEVICE (*bits, if not NULL, gets the word; bits as in moe_get_status),
+ * MOE_ECUDA or MOE_ENODEVICE. Allocates nothing.
+ */
+int moe_get_status_static(void* stream, uint32_t* bits);
 
 /*
  * ---------------------------------------------------------------------------

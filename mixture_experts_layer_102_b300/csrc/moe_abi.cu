@@ -6,6 +6,8 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <atomic>
+
 #include "../../include/moe.h"
 #include "internal.h"
 
@@ -508,18 +510,19 @@ static __device__ __align__(256) uint8_t g_route_scratch[kStaticScratchBytes];
 
 // Device address of g_route_scratch on the current device. In host code the
 // array's name is only a host-side stand-in, so the address is looked up once per
-// device (with that device current) and cached.
+// device (with that device current) and cached. Two threads making the first call on
+// one device may both look it up; they store the same address.
 int static_scratch(uint8_t** out) {
-  static void* addr[64] = {nullptr};
+  static std::atomic<void*> addr[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ECUDA;
-  if (addr[dev] == nullptr) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_route_scratch) != cudaSuccess || p == nullptr)
+  void* a = addr[dev].load(std::memory_order_acquire);
+  if (a == nullptr) {
+    if (cudaGetSymbolAddress(&a, g_route_scratch) != cudaSuccess || a == nullptr)
       return MOE_ECUDA;
-    addr[dev] = p;
+    addr[dev].store(a, std::memory_order_release);
   }
-  *out = static_cast<uint8_t*>(addr[dev]);
+  *out = static_cast<uint8_t*>(a);
   return MOE_OK;
 }
 
@@ -660,20 +663,37 @@ int moe_forward_ex(const moe_cfg* cfg, const moe_options* opts, const void* x,
                       workspace_bytes, stream, stage_events);
 }
 
-int moe_get_status(void* workspace, size_t workspace_bytes, void* stream, uint32_t* bits) {
-  if (workspace == nullptr || !aligned(workspace, kAlign) || workspace_bytes < (size_t)kStatusBytes)
-    return MOE_EWORKSPACE;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
+namespace moe {
+namespace {
+// Synchronise `stream`, then read and clear the status word at `word_addr`.
+int read_status(void* word_addr, cudaStream_t s, uint32_t* bits) {
   uint32_t word = 0;
   if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ECUDA;
-  if (cudaMemcpy(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess)
+  if (cudaMemcpy(&word, word_addr, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess)
     return MOE_ECUDA;
   if (bits != nullptr) *bits = word;
   if (word != 0) {
-    if (cudaMemset(workspace, 0, sizeof(word)) != cudaSuccess) return MOE_ECUDA;
+    if (cudaMemset(word_addr, 0, sizeof(word)) != cudaSuccess) return MOE_ECUDA;
     return MOE_EDEVICE;
   }
   return MOE_OK;
+}
+}  // namespace
+}  // namespace moe
+
+int moe_get_status(void* workspace, size_t workspace_bytes, void* stream, uint32_t* bits) {
+  if (workspace == nullptr || !aligned(workspace, kAlign) || workspace_bytes < (size_t)kStatusBytes)
+    return MOE_EWORKSPACE;
+  return read_status(workspace, static_cast<cudaStream_t>(stream), bits);
+}
+
+int moe_get_status_static(void* stream, uint32_t* bits) {
+  int rc = device_check();
+  if (rc != MOE_OK) return rc;
+  uint8_t* ws = nullptr;
+  rc = static_scratch(&ws);
+  if (rc != MOE_OK) return rc;
+  return read_status(ws, static_cast<cudaStream_t>(stream), bits);
 }
 
 const char* moe_strerror(int status) {

@@ -37,6 +37,7 @@ _SIGNATURES = {
     "moe_forward_timed": (ctypes.c_int, [_P] + [_P] * 13 + [_P, ctypes.c_size_t, _P, _P]),
     "moe_get_status": (ctypes.c_int, [_P, ctypes.c_size_t, _P, ctypes.POINTER(ctypes.c_uint32)]),
     "moe_route_static": (ctypes.c_int, [_P] + [_P] * 9 + [_P]),
+    "moe_get_status_static": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_uint32)]),
     "moe_workspace_size_ex": (ctypes.c_size_t, [_P, _P]),
     "moe_describe": (ctypes.c_int, [_P, _P, ctypes.c_int, _P]),
     "moe_route_ex": (ctypes.c_int, [_P, _P] + [_P] * 9 + [_P, ctypes.c_size_t, _P]),

@@ -3,7 +3,8 @@ hosts and serving runtimes that plan every device buffer themselves and do not l
 a kernel library call cudaMalloc). Its scratch is a static device array inside the
 library; these tests check that it gives the same routing as moe_route, which uses a
 caller-provided workspace, on two calls in a row (the array keeps the previous
-call's contents), and that a layer too large for the array is refused on the host.
+call's contents), that moe_get_status_static finds no failure reported after each
+call, and that a layer too large for the array is refused on the host.
 
 This file is collected last so that a failure here, in a run that stops at the first
 failure, comes after every other test has run.
@@ -19,6 +20,13 @@ from mixture_experts_layer_102_b300.configs import MoEConfig
 
 TOL_W = 1e-5     # gate weights, as in the parity tests
 TOL_AUX = 1e-5   # aux loss, as in the parity tests
+
+
+def _status_static():
+    bits = ctypes.c_uint32(0xFFFFFFFF)
+    rc = moe.library().moe_get_status_static(torch.cuda.current_stream().cuda_stream,
+                                             ctypes.byref(bits))
+    return rc, bits.value
 
 
 def _route_static(c, dev, r):
@@ -50,7 +58,7 @@ def test_static_route_matches_workspace_route(cfg):
     for _ in range(2):
         got = moe.new_routing(c)
         assert _route_static(c, dev, got) == moe.MOE_OK
-        torch.cuda.synchronize()
+        assert _status_static() == (moe.MOE_OK, 0)   # no kernel reported a failure
         assert (got.topk_idx == ref.topk_idx).all()
         assert (got.topk_w - ref.topk_w).abs().max().item() <= TOL_W
         assert abs(got.aux_loss.item() - ref.aux_loss.item()) <= TOL_AUX
