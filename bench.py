@@ -4,10 +4,17 @@
 
 One step is one whole forward of the layer (router, top-k and softmax, aux loss,
 capacity, dispatch, both expert GEMMs, combine) on one batch of synthetic input that
-is already resident in HBM. Inputs are larger than L2 (the expert weights) and the L2
-is flushed (a 256 MiB write) between timed steps, outside the timed events. Each step
-is timed on the device with CUDA events recorded by the library between its stages
-(moe_forward_timed), which also gives every kernel's time for the roofline.
+is already resident in HBM. The headline workload is the Mixtral-shaped layer
+(T=8192, H=4096, 8 experts, top-2, F=14336, CF 1.5), the largest named workload.
+Inputs are larger than L2 (the expert weights) and the L2 is flushed (a 256 MiB
+write) between timed steps, outside the timed events. Each step is one
+`moe_forward` call bracketed by two CUDA events on the launching stream; `value` is
+tokens over the mean step time, and the step-time distribution is printed beside it.
+A second pass of forwards through `moe_forward_timed` (an event between every two
+stages) gives each kernel's time for the roofline. The other named bf16 workloads
+(the 16-expert T=4096 layer, the fine-grained Zipf-skewed layer and the decode-size
+layer) are timed the same way in the same process and reported under
+`other_workloads`.
 
 Under torchrun (N > 1) every rank holds all experts and runs its own independent
 batch of T tokens (the same weights, activations drawn from a per-rank seed): the
@@ -42,7 +49,9 @@ UNIT = "tokens/s"
 # Buffer sets of the pipelined end-to-end loop: with three, the copy-in of a step
 # waits for the forward three steps back, not for the one just before it.
 E2E_BUFFERS = 3
-DEFAULT_CONFIG = configs.BF16_T4096
+DEFAULT_CONFIG = configs.MIXTRAL_T8192
+# timed after the headline workload in the same process (one GPU only)
+OTHER_WORKLOADS = [configs.BF16_T4096, configs.FINEGRAINED_T16384, configs.DECODE_T64]
 FLUSH_BYTES = 256 << 20
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 STAGES = ["router_logits", "route_select", "dispatch", "gemm1_swiglu", "gemm2", "combine"]
@@ -72,6 +81,8 @@ def parse_args(argv=None):
     ap.add_argument("--impl", default="mine", choices=["mine", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-others", action="store_true",
+                    help="time only the --config workload")
     ap.add_argument("--cpu-budget-s", type=float, default=10.0)
     return ap.parse_args(argv)
 
@@ -187,7 +198,10 @@ def traffic_record(kernel: str, cfg_name: str):
 # ----------------------------------------------------------------------- clocks
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+    """nvidia-smi clocks and throttle reasons, sampled every 100 ms around the timed
+    region; `stop(window)` summarises the samples whose timestamps fall inside the
+    host wall-clock window of the timed steps (the nearest sample when the window is
+    shorter than the sampling period)."""
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -201,13 +215,13 @@ class ClockSampler:
         try:
             self.out = open(f"/tmp/moe_clocks_{os.getpid()}.csv", "w")
             self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu=timestamp,{self.QUERY}",
                  "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=self.out, stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
 
-    def stop(self):
+    def stop(self, window=None):
         if self.proc is None:
             return None
         self.proc.terminate()
@@ -219,7 +233,33 @@ class ClockSampler:
         with open(self.out.name) as f:
             lines = f.readlines()
         os.unlink(self.out.name)
-        return self.summarise(lines)
+        return self.summarise_window(lines, window)
+
+    @staticmethod
+    def summarise_window(lines, window=None):
+        """`lines` start with nvidia-smi's timestamp (local time); keep the samples
+        inside `window` (t0, t1) in seconds since the epoch, else the one nearest to
+        it, and summarise them."""
+        import datetime
+        stamped = []
+        for line in lines:
+            ts, _, rest = line.partition(",")
+            try:
+                t = datetime.datetime.strptime(ts.strip(), "%Y/%m/%d %H:%M:%S.%f").timestamp()
+            except ValueError:
+                continue
+            stamped.append((t, rest.strip() + "\n"))
+        if window is not None and stamped:
+            t0, t1 = window
+            inside = [r for t, r in stamped if t0 <= t <= t1]
+            if not inside:
+                mid = 0.5 * (t0 + t1)
+                inside = [min(stamped, key=lambda tr: abs(tr[0] - mid))[1]]
+            d = ClockSampler.summarise(inside)
+            if d is not None:
+                d["samples_in_window"] = sum(1 for t, _ in stamped if t0 <= t <= t1)
+            return d
+        return ClockSampler.summarise([r for _, r in stamped])
 
     @staticmethod
     def summarise(lines):
@@ -293,157 +333,17 @@ def time_oracle(cfg, budget_s: float) -> dict:
 
 # --------------------------------------------------------------------- GPU arm
 
-def run_gpu_arm(args, cfg):
-    import torch
-    from mixture_experts_layer_102_b300 import moe
+def step_stats(step_ms) -> dict:
+    """Distribution of the per-step device times (ms)."""
+    a = np.asarray(step_ms, dtype=np.float64)
+    return {"mean": round(float(a.mean()), 5), "min": round(float(a.min()), 5),
+            "median": round(float(np.median(a)), 5),
+            "p90": round(float(np.percentile(a, 90)), 5), "max": round(float(a.max()), 5)}
 
-    rank, world, local = dist_env()
-    torch.cuda.set_device(local)
-    device = torch.device("cuda", local)
-    init_dist(world, "nccl")
 
-    inp = inputs.make_inputs(cfg, rank=rank)
-    dev = moe.to_device(inp, device)
-    c = moe.cfg_from(cfg)
-    ws = moe.make_workspace(c, device)
-    routing = moe.new_routing(c, device)
-    out = torch.empty((cfg.T, cfg.H), dtype=dev.x.dtype, device=device)
-    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
-    stream = torch.cuda.current_stream(device)
-
-    def step(evs=None):
-        moe.forward(c, dev.x, dev.w_router, dev.router_bias, dev.w1, dev.w3, dev.w2,
-                    workspace=ws, out=out, routing=routing, stream=stream, stage_events=evs)
-
-    for _ in range(args.warmup):
-        flush.zero_()
-        step()
-    torch.cuda.synchronize(device)
-    moe.get_status(ws)
-    kept_slots = int(routing.kept_counts.sum().item())
-    touched = int((routing.kept_counts > 0).sum().item())
-
-    # Timed region: K whole forwards, each bracketed by two events on the stream (the
-    # L2 flush between steps stays outside them).
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    sampler = ClockSampler(local)
-    barrier(world, device)
-    torch.cuda.synchronize(device)
-    sampler.start()
-    time.sleep(0.3)  # let the sampler take its first readings
-    wall0 = time.perf_counter()
-    for i in range(args.steps):
-        flush.zero_()
-        starts[i].record(stream)
-        step()
-        ends[i].record(stream)
-    torch.cuda.synchronize(device)
-    wall = time.perf_counter() - wall0
-    barrier(world, device)
-    clocks = sampler.stop()
-    moe.get_status(ws)
-    step_ms = np.array([a.elapsed_time(b) for a, b in zip(starts, ends)])
-    mean_ms = float(step_ms.mean())
-    max_ms = reduce_max(mean_ms, world, device)
-    total_tokens = reduce_sum(cfg.T, world, device)
-
-    # Per-kernel times: the same forwards with an event between every two stages
-    # (moe_forward_timed). The extra event records add a little time per step, so these
-    # steps are timed apart from the ones above.
-    n_prof = min(args.steps, 200)
-    ev_sets = [moe.make_stage_events(stream) for _ in range(n_prof)]
-    torch.cuda.synchronize(device)
-    for i in range(n_prof):
-        flush.zero_()
-        step(ev_sets[i])
-    torch.cuda.synchronize(device)
-    moe.get_status(ws)
-    stage_ms = np.zeros((n_prof, len(STAGES)))
-    for i, evs in enumerate(ev_sets):
-        for s in range(len(STAGES)):
-            stage_ms[i, s] = evs[s].elapsed_time(evs[s + 1])
-
-    # End to end through the public API: every step copies its x from pinned host
-    # memory to the device and its out and aux back to pinned host memory. Pipelined
-    # as a serving loop would run it: the copy-in of step i+1 and the copy-out of step
-    # i run on their own streams beside the forward of step i (double buffers ordered
-    # by events; E2E_BUFFERS sets of buffers, so a forward waits only on the copies of
-    # the step E2E_BUFFERS back). The fully serial loop (copy, forward, copy,
-    # synchronise) is also reported.
-    e2e = None
-    if not args.no_e2e:
-        n_e2e = min(args.steps, 200)
-        b = 2 if cfg.dtype == "bf16" else 4
-        nb = E2E_BUFFERS
-        x_host = [moe.to_torch(inputs.make_x(cfg, rank=rank * 7919 + 1 + j), cfg.dtype).pin_memory()
-                  for j in range(nb)]
-        out_host = [torch.empty((cfg.T, cfg.H), dtype=dev.x.dtype).pin_memory() for _ in range(nb)]
-        aux_host = [torch.empty(1, dtype=torch.float32).pin_memory() for _ in range(nb)]
-        x_dev = [torch.empty_like(dev.x) for _ in range(nb)]
-        out_dev = [torch.empty_like(out) for _ in range(nb)]
-        rts = [moe.new_routing(c, device) for _ in range(nb)]
-        s_in = torch.cuda.Stream(device)
-        s_out = torch.cuda.Stream(device)
-        ev_in = [torch.cuda.Event() for _ in range(nb)]
-        ev_fwd = [torch.cuda.Event() for _ in range(nb)]
-        ev_out = [torch.cuda.Event() for _ in range(nb)]
-
-        def run_pipelined(n):
-            for i in range(n):
-                j = i % nb
-                with torch.cuda.stream(s_in):
-                    if i >= nb:
-                        s_in.wait_event(ev_fwd[j])        # step i-nb no longer reads x_dev[j]
-                    x_dev[j].copy_(x_host[j], non_blocking=True)
-                    ev_in[j].record(s_in)
-                stream.wait_event(ev_in[j])
-                if i >= nb:
-                    stream.wait_event(ev_out[j])          # step i-nb's out has been copied out
-                moe.forward(c, x_dev[j], dev.w_router, dev.router_bias, dev.w1, dev.w3, dev.w2,
-                            workspace=ws, out=out_dev[j], routing=rts[j], stream=stream)
-                ev_fwd[j].record(stream)
-                with torch.cuda.stream(s_out):
-                    s_out.wait_event(ev_fwd[j])
-                    out_host[j].copy_(out_dev[j], non_blocking=True)
-                    aux_host[j].copy_(rts[j].aux_loss, non_blocking=True)
-                    ev_out[j].record(s_out)
-            torch.cuda.synchronize(device)
-
-        def run_serial(n):
-            for i in range(n):
-                j = i % nb
-                x_dev[j].copy_(x_host[j], non_blocking=True)
-                moe.forward(c, x_dev[j], dev.w_router, dev.router_bias, dev.w1, dev.w3, dev.w2,
-                            workspace=ws, out=out_dev[j], routing=rts[j], stream=stream)
-                out_host[j].copy_(out_dev[j], non_blocking=True)
-                aux_host[j].copy_(rts[j].aux_loss, non_blocking=True)
-                stream.synchronize()
-
-        run_pipelined(max(3, args.warmup))
-        barrier(world, device)
-        t0 = time.perf_counter()
-        run_pipelined(n_e2e)
-        pipe_s = reduce_max((time.perf_counter() - t0) / n_e2e, world, device)
-        run_serial(3)
-        barrier(world, device)
-        t0 = time.perf_counter()
-        run_serial(n_e2e)
-        serial_s = reduce_max((time.perf_counter() - t0) / n_e2e, world, device)
-        moe.get_status(ws)
-        e2e = {"value": round(total_tokens / pipe_s, 1), "unit": UNIT,
-               "h2d_bytes_per_step": cfg.T * cfg.H * b,
-               "d2h_bytes_per_step": cfg.T * cfg.H * b + 4,
-               "ms_per_step": round(pipe_s * 1e3, 5), "steps": n_e2e,
-               "mode": f"pipelined: copy-in of step i+1 and copy-out of step i on their "
-                       f"own streams beside the forward of step i, {nb} buffer sets",
-               "serial_value": round(total_tokens / serial_s, 1),
-               "serial_ms_per_step": round(serial_s * 1e3, 5)}
-
-    if rank != 0:
-        return None
-
-    peaks, peak_src = load_peaks()
+def kernel_report(cfg, stage_ms, kept_slots: int, touched: int, peaks: dict, peak_src: str):
+    """Per-kernel time, rate and roofline fraction from the staged pass, the roofline
+    of the kernel with the largest share, and the grouped GEMM's combined rate."""
     units = algorithmic_units(cfg, kept_slots, touched)
     names = stage_names(cfg)
     if names[0] == "route":  # the router's events are back to back: merge the stages
@@ -455,7 +355,7 @@ def run_gpu_arm(args, cfg):
         flops, nbytes = units[name]
         sec = mean_stage[s] / 1e3
         bound = bound_of(flops, nbytes, peaks)
-        ent = {"ms": round(mean_stage[s], 5), "bound": bound,
+        ent = {"ms": round(float(mean_stage[s]), 5), "bound": bound,
                "GB/s": round(nbytes / sec / 1e9, 1)}
         if flops > 0:
             ent["TFLOP/s"] = round(flops / sec / 1e12, 2)
@@ -466,40 +366,267 @@ def run_gpu_arm(args, cfg):
     flops, nbytes = units[dom]
     sec = mean_stage[names.index(dom)] / 1e3
     bound = bound_of(flops, nbytes, peaks)
-    traffic = traffic_record(dom, cfg.name)
     if bound == "tensor":
         ach, peak, unit, amount = flops / sec / 1e12, peaks["bf16_tflops"], "TFLOP/s", flops
     else:
         ach, peak, unit, amount = nbytes / sec / 1e9, peaks["hbm_gbs"], "GB/s", nbytes
     roofline = {"kernel": dom, "bound": bound, "achieved": round(ach, 2), "peak": peak,
-                "unit": unit, "frac": round(ach / peak, 4), "traffic": traffic,
+                "unit": unit, "frac": round(ach / peak, 4),
+                "traffic": traffic_record(dom, cfg.name),
                 "peak_source": f"{peak_src} ({'bf16 burst' if bound == 'tensor' else 'HBM copy'})",
                 "algorithmic_per_launch": amount}
+    if bound == "tensor" and "bf16_tflops_sustained" in peaks:
+        ps = peaks["bf16_tflops_sustained"]
+        roofline["peak_sustained"] = ps
+        roofline["frac_sustained"] = round(ach / ps, 4)
     gemm_flops = units["gemm1_swiglu"][0] + units["gemm2"][0]
     gemm_sec = (mean_stage[names.index("gemm1_swiglu")] + mean_stage[names.index("gemm2")]) / 1e3
+    gtf = gemm_flops / gemm_sec / 1e12
+    grouped = {"TFLOP/s": round(gtf, 2), "frac": round(gtf / peaks["bf16_tflops"], 4)}
+    if "bf16_tflops_sustained" in peaks:
+        grouped["frac_sustained"] = round(gtf / peaks["bf16_tflops_sustained"], 4)
+    staged = round(float(stage_ms.sum(axis=1).mean()), 5)
+    return per_kernel, roofline, grouped, staged
+
+
+class Workload:
+    """One layer instance resident on the device, with its workspace and outputs."""
+
+    def __init__(self, cfg, device, rank: int = 0):
+        import torch
+        from mixture_experts_layer_102_b300 import moe
+        self.cfg = cfg
+        self.device = device
+        inp = inputs.make_inputs(cfg, rank=rank)
+        self.dev = moe.to_device(inp, device)
+        del inp
+        self.c = moe.cfg_from(cfg)
+        self.ws = moe.make_workspace(self.c, device)
+        self.routing = moe.new_routing(self.c, device)
+        self.out = torch.empty((cfg.T, cfg.H), dtype=self.dev.x.dtype, device=device)
+
+    def step(self, stream, evs=None):
+        from mixture_experts_layer_102_b300 import moe
+        d = self.dev
+        moe.forward(self.c, d.x, d.w_router, d.router_bias, d.w1, d.w3, d.w2,
+                    workspace=self.ws, out=self.out, routing=self.routing, stream=stream,
+                    stage_events=evs)
+
+
+def time_steps(wl, steps: int, warmup: int, stream, flush, world: int, device):
+    """`warmup` untimed forwards directly before `steps` timed ones, each timed one
+    bracketed by two events on the stream with an L2 flush between steps (outside the
+    events). Returns the per-step ms and the host wall-clock window of the timed loop."""
+    import torch
+    from mixture_experts_layer_102_b300 import moe
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    barrier(world, device)
+    for _ in range(warmup):
+        flush.zero_()
+        wl.step(stream)
+    torch.cuda.synchronize(device)
+    moe.get_status(wl.ws)
+    barrier(world, device)
+    torch.cuda.synchronize(device)
+    t0 = time.time()
+    for i in range(steps):
+        flush.zero_()
+        starts[i].record(stream)
+        wl.step(stream)
+        ends[i].record(stream)
+    torch.cuda.synchronize(device)
+    t1 = time.time()
+    barrier(world, device)
+    moe.get_status(wl.ws)
+    step_ms = np.array([a.elapsed_time(b) for a, b in zip(starts, ends)])
+    return step_ms, (t0, t1)
+
+
+def staged_pass(wl, n: int, stream, flush, device):
+    """Per-stage ms of `n` forwards through moe_forward_timed ([n, stages])."""
+    import torch
+    from mixture_experts_layer_102_b300 import moe
+    ev_sets = [moe.make_stage_events(stream) for _ in range(n)]
+    torch.cuda.synchronize(device)
+    for i in range(n):
+        flush.zero_()
+        wl.step(stream, ev_sets[i])
+    torch.cuda.synchronize(device)
+    moe.get_status(wl.ws)
+    stage_ms = np.zeros((n, len(STAGES)))
+    for i, evs in enumerate(ev_sets):
+        for s in range(len(STAGES)):
+            stage_ms[i, s] = evs[s].elapsed_time(evs[s + 1])
+    return stage_ms
+
+
+def time_e2e(wl, args, stream, device, rank: int, world: int, total_tokens: float):
+    """End to end through the public API: every step copies its x from pinned host
+    memory to the device and its out and aux back to pinned host memory. Pipelined as
+    a serving loop would run it: the copy-in of step i+1 and the copy-out of step i run
+    on their own streams beside the forward of step i (buffers ordered by events;
+    E2E_BUFFERS sets of buffers, so a forward waits only on the copies of the step
+    E2E_BUFFERS back). The fully serial loop (copy, forward, copy, synchronise) is also
+    reported."""
+    import torch
+    from mixture_experts_layer_102_b300 import moe
+    cfg, c, dev = wl.cfg, wl.c, wl.dev
+    n_e2e = min(args.steps, 200)
+    b = 2 if cfg.dtype == "bf16" else 4
+    nb = E2E_BUFFERS
+    x_host = [moe.to_torch(inputs.make_x(cfg, rank=rank * 7919 + 1 + j), cfg.dtype).pin_memory()
+              for j in range(nb)]
+    out_host = [torch.empty((cfg.T, cfg.H), dtype=dev.x.dtype).pin_memory() for _ in range(nb)]
+    aux_host = [torch.empty(1, dtype=torch.float32).pin_memory() for _ in range(nb)]
+    x_dev = [torch.empty_like(dev.x) for _ in range(nb)]
+    out_dev = [torch.empty_like(wl.out) for _ in range(nb)]
+    rts = [moe.new_routing(c, device) for _ in range(nb)]
+    s_in = torch.cuda.Stream(device)
+    s_out = torch.cuda.Stream(device)
+    ev_in = [torch.cuda.Event() for _ in range(nb)]
+    ev_fwd = [torch.cuda.Event() for _ in range(nb)]
+    ev_out = [torch.cuda.Event() for _ in range(nb)]
+
+    def fwd(j):
+        moe.forward(c, x_dev[j], dev.w_router, dev.router_bias, dev.w1, dev.w3, dev.w2,
+                    workspace=wl.ws, out=out_dev[j], routing=rts[j], stream=stream)
+
+    def run_pipelined(n):
+        for i in range(n):
+            j = i % nb
+            with torch.cuda.stream(s_in):
+                if i >= nb:
+                    s_in.wait_event(ev_fwd[j])        # step i-nb no longer reads x_dev[j]
+                x_dev[j].copy_(x_host[j], non_blocking=True)
+                ev_in[j].record(s_in)
+            stream.wait_event(ev_in[j])
+            if i >= nb:
+                stream.wait_event(ev_out[j])          # step i-nb's out has been copied out
+            fwd(j)
+            ev_fwd[j].record(stream)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev_fwd[j])
+                out_host[j].copy_(out_dev[j], non_blocking=True)
+                aux_host[j].copy_(rts[j].aux_loss, non_blocking=True)
+                ev_out[j].record(s_out)
+        torch.cuda.synchronize(device)
+
+    def run_serial(n):
+        for i in range(n):
+            j = i % nb
+            x_dev[j].copy_(x_host[j], non_blocking=True)
+            fwd(j)
+            out_host[j].copy_(out_dev[j], non_blocking=True)
+            aux_host[j].copy_(rts[j].aux_loss, non_blocking=True)
+            stream.synchronize()
+
+    run_pipelined(max(3, args.warmup))
+    barrier(world, device)
+    t0 = time.perf_counter()
+    run_pipelined(n_e2e)
+    pipe_s = reduce_max((time.perf_counter() - t0) / n_e2e, world, device)
+    run_serial(3)
+    barrier(world, device)
+    t0 = time.perf_counter()
+    run_serial(n_e2e)
+    serial_s = reduce_max((time.perf_counter() - t0) / n_e2e, world, device)
+    moe.get_status(wl.ws)
+    return {"value": round(total_tokens / pipe_s, 1), "unit": UNIT,
+            "h2d_bytes_per_step": cfg.T * cfg.H * b,
+            "d2h_bytes_per_step": cfg.T * cfg.H * b + 4,
+            "ms_per_step": round(pipe_s * 1e3, 5), "steps": n_e2e,
+            "mode": f"pipelined: copy-in of step i+1 and copy-out of step i on their "
+                    f"own streams beside the forward of step i, {nb} buffer sets",
+            "serial_value": round(total_tokens / serial_s, 1),
+            "serial_ms_per_step": round(serial_s * 1e3, 5)}
+
+
+def measure_workload(cfg, args, device, stream, flush, rank, world, peaks, peak_src,
+                     clocks=False, e2e=False):
+    """Time one workload: the timed forwards, the staged pass, optionally the clocks of
+    the timed window and the end-to-end loop. Frees its device memory on return."""
+    import torch
+    from mixture_experts_layer_102_b300 import moe
+    wl = Workload(cfg, device, rank)
+    torch.cuda.synchronize(device)
+    sampler = ClockSampler(device.index) if clocks else None
+    if sampler is not None:
+        sampler.start()
+        time.sleep(0.3)  # the sampler's first readings come before the warm-up
+    step_ms, window = time_steps(wl, args.steps, args.warmup, stream, flush, world, device)
+    clock = sampler.stop(window) if sampler is not None else None
+    kept_slots = int(wl.routing.kept_counts.sum().item())
+    touched = int((wl.routing.kept_counts > 0).sum().item())
+    mean_ms = reduce_max(float(step_ms.mean()), world, device)
+    total_tokens = reduce_sum(cfg.T, world, device)
+    stage_ms = staged_pass(wl, min(args.steps, 200), stream, flush, device)
+    e2e_rec = time_e2e(wl, args, stream, device, rank, world, total_tokens) if e2e else None
+    per_kernel, roofline, grouped, staged = kernel_report(cfg, stage_ms, kept_slots, touched,
+                                                          peaks, peak_src)
+    rec = {"value": round(total_tokens / (mean_ms / 1e3), 1), "ms_per_step": round(mean_ms, 5),
+           "step_ms": step_stats(step_ms), "kept_slots": kept_slots, "touched_experts": touched,
+           "global_tokens": int(total_tokens), "grouped_gemm": grouped, "kernels": per_kernel,
+           "staged_ms_per_step": staged, "roofline": roofline,
+           "gpu_launches": launches_per_forward(cfg) * args.steps,
+           "plan": moe.describe(wl.c, has_bias=wl.dev.router_bias is not None),
+           "wall_s_timed_region": round(window[1] - window[0], 3)}
+    if clocks:
+        rec["clocks"] = clock
+    if e2e:
+        rec["e2e"] = e2e_rec
+    del wl
+    torch.cuda.synchronize(device)
+    torch.cuda.empty_cache()
+    return rec
+
+
+def cfg_record(cfg, world: int) -> dict:
+    return {"workload": cfg.name, "T": cfg.T, "H": cfg.H, "N": cfg.N, "k": cfg.k, "F": cfg.F,
+            "capacity_factor": cfg.capacity_factor, "router_bias": "zipf" if cfg.zipf_bias else None,
+            "parallelism": f"dp{world} (independent batches, no collective)",
+            "l2": "flushed between steps (256 MiB write); weights exceed L2"}
+
+
+def run_gpu_arm(args, cfg):
+    import torch
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    init_dist(world, "nccl")
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream(device)
+    peaks, peak_src = load_peaks()
+
+    head = measure_workload(cfg, args, device, stream, flush, rank, world, peaks, peak_src,
+                            clocks=True, e2e=not args.no_e2e)
+    others = {}
+    if world == 1 and not args.no_others:
+        for oc in OTHER_WORKLOADS:
+            if oc.name == cfg.name:
+                continue
+            rec = measure_workload(oc, args, device, stream, flush, rank, world, peaks,
+                                   peak_src)
+            rec["config"] = cfg_record(oc, world)
+            others[oc.name] = rec
+    if rank != 0:
+        return None
+    conf = cfg_record(cfg, world)
+    conf.update(kept_slots=head.pop("kept_slots"), touched_experts=head.pop("touched_experts"),
+                global_tokens=head.pop("global_tokens"))
     result = {
-        "metric": METRIC, "value": round(total_tokens / (max_ms / 1e3), 1), "unit": UNIT,
+        "metric": METRIC, "value": head.pop("value"), "unit": UNIT,
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": round(max_ms, 5), "higher_is_better": True, "scaling": "weak",
+        "ms_per_step": head.pop("ms_per_step"), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": cfg.dtype, "data": "synthetic (seeded, random-init weights)",
-        "config": {"workload": cfg.name, "T": cfg.T, "H": cfg.H, "N": cfg.N, "k": cfg.k,
-                   "F": cfg.F, "capacity_factor": cfg.capacity_factor,
-                   "kept_slots": kept_slots, "touched_experts": touched,
-                   "global_tokens": int(total_tokens),
-                   "parallelism": f"dp{world} (independent batches, no collective)",
-                   "l2": "flushed between steps (256 MiB write); weights exceed L2"},
-        "grouped_gemm": {"TFLOP/s": round(gemm_flops / gemm_sec / 1e12, 2),
-                         "frac": round(gemm_flops / gemm_sec / 1e12 / peaks["bf16_tflops"], 4)},
-        "kernels": per_kernel,
-        "kernels_note": "per-kernel ms from separate steps with an event between stages",
-        "staged_ms_per_step": round(float(stage_ms.sum(axis=1).mean()), 5),
-        "roofline": roofline,
-        "gpu_launches": launches_per_forward(cfg) * args.steps,
-        "plan": moe.describe(c, has_bias=dev.router_bias is not None),
-        "clocks": clocks,
-        "wall_s_timed_region": round(wall, 3),
-        "e2e": e2e,
+        "config": conf,
     }
+    result.update(head)
+    result["kernels_note"] = ("per-kernel ms from separate forwards with an event between "
+                              "stages (moe_forward_timed); value and step_ms from whole "
+                              "moe_forward calls")
+    result["other_workloads"] = others if others else None
     return result
 
 

@@ -9,7 +9,8 @@ The five named workloads follow the shapes the pages discuss: a tiny fp32 layer,
 with hot experts forced by a router bias (2kiu.com/news/2885792, section 5.2, cools
 hot experts with a per-expert logit offset; the same mechanism is used here to make
 them hot), and a decode-size 100-expert top-2 layer, i.e. 2% of the experts active
-(devpress.csdn.net "GPT-4 uses 2%", section 3.2).
+(the devpress.csdn.net MoE page, section 3.2, puts the active share of a large
+model's parameters at 2%).
 
 This module holds data only: no part of the layer's arithmetic lives here.
 """

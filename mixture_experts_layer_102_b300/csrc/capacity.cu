@@ -4,7 +4,7 @@
 //
 // Each expert keeps its first C routed slots in token order and the rest are dropped
 // to the residual (cf-1.com/news/5914943 section 2.3 note; 2kiu.com/news/2885792
-// section 3.1 keeps "the first capacity tokens" per expert, section 2.2 capacity
+// section 3.1 keeps each expert's earliest tokens up to its capacity, section 2.2 capacity
 // factor). Kept slots go to row offsets[e] + rank of the permuted buffer ("scatter
 // tokens into expert queues", devpress.csdn.net MoE page section 4.1), copied with
 // 16-byte vectors, one warp per token.

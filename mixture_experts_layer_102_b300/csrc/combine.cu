@@ -1,7 +1,7 @@
 // Gate-weighted combine: out[t] = sum over kept slots s of w[t,s] * ye[row(t,s)]
-// (cf-1.com/news/5914943 section 2.1: "weighted sum of the k experts' outputs";
-// devpress.csdn.net MoE page section 4.1: gather the expert results back into token
-// order). Dropped slots contribute nothing and the kept slots keep their weights;
+// (cf-1.com/news/5914943 section 2.1 sums the k experts' outputs weighted by the
+// gates; devpress.csdn.net MoE page section 4.1 gathers the expert results back into
+// token order). Dropped slots contribute nothing and the kept slots keep their weights;
 // the residual is added by the caller (cf-1.com/news/5914943 section 2.3 note).
 //
 // Shared experts (hotelren.com/news/5904824 section 3.3) are slots k..k+S-1 with

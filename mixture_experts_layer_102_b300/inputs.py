@@ -33,6 +33,7 @@ arithmetic.
 """
 from __future__ import annotations
 
+from concurrent.futures import ThreadPoolExecutor
 from dataclasses import dataclass
 from typing import Optional
 
@@ -42,10 +43,25 @@ from .configs import MoEConfig
 
 
 def f32_to_bf16_bits(a: np.ndarray) -> np.ndarray:
-    """Round finite float32 values to bf16 (nearest, ties to even); return the bits."""
+    """Round finite float32 values to bf16 (nearest, ties to even); return the bits.
+    Large arrays are converted in chunks on a few threads (same result)."""
     u = np.ascontiguousarray(a, dtype=np.float32).view(np.uint32)
-    lsb = (u >> np.uint32(16)) & np.uint32(1)
-    return ((u + np.uint32(0x7FFF) + lsb) >> np.uint32(16)).astype(np.uint16)
+    flat = u.reshape(-1)
+    out = np.empty(flat.shape, dtype=np.uint16)
+
+    def part(lo, hi):
+        v = flat[lo:hi]
+        lsb = (v >> np.uint32(16)) & np.uint32(1)
+        out[lo:hi] = (v + np.uint32(0x7FFF) + lsb) >> np.uint32(16)
+
+    chunk = 1 << 24
+    if flat.size <= chunk:
+        part(0, flat.size)
+    else:
+        with ThreadPoolExecutor(max_workers=8) as ex:
+            list(ex.map(lambda lo: part(lo, min(lo + chunk, flat.size)),
+                        range(0, flat.size, chunk)))
+    return out.reshape(u.shape)
 
 
 def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
@@ -122,9 +138,11 @@ def make_inputs(cfg: MoEConfig, rank: int = 0, with_experts: bool = True,
         r = g.permutation(N).astype(np.float64) + 1.0
         bias = (2.0 * r ** -1.1).astype(np.float32)
     if with_experts:
-        w1 = _store(_normal(seqs[3], (NE, F, H), H ** -0.5), cfg.dtype)
-        w3 = _store(_normal(seqs[4], (NE, F, H), H ** -0.5), cfg.dtype)
-        w2 = _store(_normal(seqs[5], (NE, H, F), F ** -0.5), cfg.dtype)
+        # one stream per tensor, so the three draws may run side by side
+        jobs = [(seqs[3], (NE, F, H), H ** -0.5), (seqs[4], (NE, F, H), H ** -0.5),
+                (seqs[5], (NE, H, F), F ** -0.5)]
+        with ThreadPoolExecutor(max_workers=3) as ex:
+            w1, w3, w2 = ex.map(lambda j: _store(_normal(*j), cfg.dtype), jobs)
     else:
         w1 = w3 = w2 = None
     return MoEInputs(cfg.dtype, x, w_router, bias, w1, w3, w2)
