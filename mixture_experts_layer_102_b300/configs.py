@@ -52,7 +52,14 @@ DECODE_T64 = MoEConfig("decode_t64_h4096_n100_k2_f2048", 64, 4096, 100, 2, 2048,
                        "bf16")
 
 NAMED = [TINY_F32, BF16_T4096, MIXTRAL_T8192, FINEGRAINED_T16384, DECODE_T64]
-BY_NAME = {c.name: c for c in NAMED}
+
+# A profiling case with the Mixtral-shaped layer's per-expert geometry (about 2048 rows
+# per expert, H=4096, F=14336) but two experts: 0.7 GB of weights instead of 2.8 GB,
+# small enough for multi-pass profiler captures.
+MIXTRAL_GEOMETRY_T2048 = MoEConfig("mixtral_geometry_t2048_h4096_n2_k2_f14336_cf1.5", 2048,
+                                   4096, 2, 2, 14336, 1.5, "bf16")
+
+BY_NAME = {c.name: c for c in NAMED + [MIXTRAL_GEOMETRY_T2048]}
 
 # Short aliases used on command lines.
 ALIASES = {
@@ -61,6 +68,7 @@ ALIASES = {
     "mixtral": MIXTRAL_T8192.name,
     "finegrained": FINEGRAINED_T16384.name,
     "decode": DECODE_T64.name,
+    "mixtral_geometry": MIXTRAL_GEOMETRY_T2048.name,
 }
 
 

@@ -7,8 +7,9 @@
 // Shared experts (hotelren.com/news/5904824 section 3.3) are slots k..k+S-1 with
 // weight 1; a padding token has no row in any slot and gets 0.
 //
-// One warp per token, 16-byte vectors, fp32 accumulation in a fixed slot order so
-// the result does not depend on scheduling.
+// One warp per token, 16-byte vectors. The loads of two slots' rows are in flight
+// together, held as loaded until they are added; accumulation is fp32 in a fixed slot
+// order, so the result does not depend on scheduling.
 #include "common.cuh"
 #include "internal.h"
 
@@ -38,9 +39,10 @@ combine_kernel(const TIo* __restrict__ ye, const int32_t* __restrict__ slot_row,
   pdl_trigger();
   if (t >= T) return;
   __syncwarp();
-  // Groups of 8 elements (one 16-byte bf16 vector); each lane keeps VPL groups in
-  // flight per slot so the loads of a slot overlap.
-  constexpr int VPL = 4;
+  // Groups of 8 elements (one 16-byte bf16 vector); each lane keeps VPL groups of two
+  // slots in flight at once, held as loaded until they are added in slot order.
+  constexpr int VPL = 4, SG = 2;
+  constexpr int N16 = (int)sizeof(TIo) * 8 / 16;
   const int ngrp = H / 8;
   for (int g0 = 0; g0 < ngrp; g0 += 32 * VPL) {
     float acc[VPL][8];
@@ -48,23 +50,45 @@ combine_kernel(const TIo* __restrict__ ye, const int32_t* __restrict__ slot_row,
     for (int u = 0; u < VPL; ++u)
 #pragma unroll
       for (int q = 0; q < 8; ++q) acc[u][q] = 0.f;
-    for (int s = 0; s < slots; ++s) {
-      const int r = rows[warp][s];
-      if (r < 0) continue;
-      const float ws = wts[warp][s];
-      const TIo* src = ye + (size_t)r * H;
-      float val[VPL][8];
+    for (int s0 = 0; s0 < slots; s0 += SG) {
+      uint4 raw[SG][VPL][N16];
 #pragma unroll
-      for (int u = 0; u < VPL; ++u) {
-        const int g = g0 + u * 32 + lane;
-        if (g < ngrp) load8(src + g * 8, val[u]);
+      for (int j = 0; j < SG; ++j) {
+        const int r = s0 + j < slots ? rows[warp][s0 + j] : -1;
+        if (r < 0) continue;
+        const TIo* src = ye + (size_t)r * H;
+#pragma unroll
+        for (int u = 0; u < VPL; ++u) {
+          const int g = g0 + u * 32 + lane;
+          if (g < ngrp)
+#pragma unroll
+            for (int i = 0; i < N16; ++i) raw[j][u][i] = reinterpret_cast<const uint4*>(src + g * 8)[i];
+        }
       }
 #pragma unroll
-      for (int u = 0; u < VPL; ++u) {
-        const int g = g0 + u * 32 + lane;
-        if (g < ngrp) {
+      for (int j = 0; j < SG; ++j) {
+        const int r = s0 + j < slots ? rows[warp][s0 + j] : -1;
+        if (r < 0) continue;
+        const float ws = wts[warp][s0 + j];
 #pragma unroll
-          for (int q = 0; q < 8; ++q) acc[u][q] = fmaf(ws, val[u][q], acc[u][q]);
+        for (int u = 0; u < VPL; ++u) {
+          const int g = g0 + u * 32 + lane;
+          if (g < ngrp) {
+            if constexpr (sizeof(TIo) == 2) {
+              const uint32_t v[4] = {raw[j][u][0].x, raw[j][u][0].y, raw[j][u][0].z, raw[j][u][0].w};
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                acc[u][2 * q] = fmaf(ws, bf16_lo(v[q]), acc[u][2 * q]);
+                acc[u][2 * q + 1] = fmaf(ws, bf16_hi(v[q]), acc[u][2 * q + 1]);
+              }
+            } else {
+              const uint32_t v[8] = {raw[j][u][0].x, raw[j][u][0].y, raw[j][u][0].z, raw[j][u][0].w,
+                                     raw[j][u][N16 - 1].x, raw[j][u][N16 - 1].y,
+                                     raw[j][u][N16 - 1].z, raw[j][u][N16 - 1].w};
+#pragma unroll
+              for (int q = 0; q < 8; ++q) acc[u][q] = fmaf(ws, __uint_as_float(v[q]), acc[u][q]);
+            }
+          }
         }
       }
     }

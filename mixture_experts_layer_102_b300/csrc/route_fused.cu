@@ -222,11 +222,15 @@ route_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
   }
   // ------------------------------------------- per-token decisions (all 8 warps)
   // Two threads per token, adjacent lanes: thread h of token r takes the experts of
-  // parity h. Every thread runs the max, the sum and the picks (so the pair's shuffles
-  // are never divergent); only live tokens write. Any timeout (abort flag) leaves every
-  // token of the tile without a decision, as padding.
+  // parity h. Every thread runs the picks and the sum (so the pair's shuffles are
+  // never divergent); only live tokens write. Any timeout (abort flag) leaves every
+  // token of the tile without a decision, as padding. Passes over the token's experts:
+  // k picks (the first also clears the selection marks, and its value is the row's
+  // maximum), then one pass that turns each logit into exp(l - max), summing them.
+  // The probabilities are those values times 1/sum, applied where they are read.
   const bool masked = a.valid != nullptr;
   const bool want_d2 = a.aux_std2 != nullptr;
+  __shared__ float s_inv[TOK];  // 1/sum of each token's exponentials (0: not live)
   float d2 = 0.f;
   {
     const unsigned FULL = 0xffffffffu;
@@ -235,21 +239,11 @@ route_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
     float* row = L + r * LS;
     uint8_t* ch = CH + (size_t)r * N;
     int32_t* sel = SEL + r * k;
-    for (int e = h; e < N; e += 2) ch[e] = 0;
     const bool live = *abort_flag == 0 && t < a.T && (!masked || a.valid[t] != 0);
     if (h == 0) s_valid[r] = live ? 1 : 0;
-    float m = -INFINITY;
-#pragma unroll 8
-    for (int e = h; e < N; e += 2) m = fmaxf(m, row[e]);
-    m = fmaxf(m, __shfl_xor_sync(FULL, m, 1));
-    float sum = 0.f;
-#pragma unroll 8
-    for (int e = h; e < N; e += 2) sum += expf(row[e] - m);
-    sum += __shfl_xor_sync(FULL, sum, 1);  // the same sum on both threads
-    const float inv = 1.f / sum;
     // top k: pick j is the best logit strictly after pick j-1 in (logit desc, id asc);
     // each thread scans its parity, and the pair keeps the better of its two candidates
-    float pl = INFINITY, l0 = 0.f, zs = 0.f;
+    float pl = INFINITY, l0 = 0.f, zs = 0.f, m = -INFINITY;
     int pi = -1;
     for (int j = 0; j < k; ++j) {
       float bv = -INFINITY;
@@ -257,6 +251,7 @@ route_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
 #pragma unroll 8
       for (int e = h; e < N; e += 2) {
         const float v = row[e];
+        if (j == 0) ch[e] = 0;
         const bool after = v < pl || (v == pl && e > pi);
         if (after && (bi < 0 || v > bv)) {
           bv = v;
@@ -269,6 +264,7 @@ route_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
         bv = ov;
         bi = oi;
       }
+      if (j == 0 && bi >= 0) m = bv;  // the largest logit of the row
       if (bi < 0) {  // only NaN logits leave no candidate: keep the index in range
         bi = j;
         bv = row[j];
@@ -279,7 +275,7 @@ route_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
       pl = bv;
       pi = bi;
     }
-    __syncwarp();  // the pair's picks and zeroed marks are in place
+    __syncwarp();  // the pair's picks and cleared marks are in place
     if (live) {
       for (int j = h; j < k; j += 2) {  // gate weights: softmax over the k selected logits
         const int e = sel[j];
@@ -294,12 +290,23 @@ route_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
       }
     }
     __syncwarp();  // the gates have read the logits they need
-    const float invN = 1.f / (float)N;
+    float sum = 0.f;
 #pragma unroll 8
-    for (int e = h; e < N; e += 2) {  // the token's probabilities replace its logits
-      const float pe = live ? expf(row[e] - m) * inv : 0.f;
-      row[e] = pe;
-      if (want_d2 && live) d2 = fmaf(pe - invN, pe - invN, d2);
+    for (int e = h; e < N; e += 2) {  // exp(l - max) replaces each logit
+      const float x = live ? expf(row[e] - m) : 0.f;
+      row[e] = x;
+      sum += x;
+    }
+    sum += __shfl_xor_sync(FULL, sum, 1);  // the same sum on both threads
+    const float inv = 1.f / sum;
+    if (h == 0) s_inv[r] = live ? inv : 0.f;
+    if (want_d2 && live) {
+      const float invN = 1.f / (float)N;
+#pragma unroll 8
+      for (int e = h; e < N; e += 2) {
+        const float pe = __fmul_rn(row[e], inv);
+        d2 = fmaf(pe - invN, pe - invN, d2);
+      }
     }
   }
   __syncthreads();
@@ -320,7 +327,7 @@ route_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
     const bool mine = e < N && g < G;
     if (mine) {
       for (int r = g * R; r < g * R + R; ++r) {
-        ps += L[r * LS + e];
+        ps += __fmul_rn(L[r * LS + e], s_inv[r]);  // the token's probability of e
         cnt += CH[(size_t)r * N + e] != 0;
       }
       s_gc[g * np2 + e] = cnt;
