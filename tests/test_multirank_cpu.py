@@ -166,3 +166,16 @@ def test_traffic_record_follows_the_captured_sources(tmp_path, monkeypatch):
     assert bench.traffic_record("gemm1_swiglu", "wl") is None
     src.unlink()
     assert bench.traffic_record("gemm1_swiglu", "wl") is None
+
+
+def test_tensor_peak_follows_the_power_regime_of_the_timed_region():
+    # a tensor-bound kernel timed inside a power-capped loop is measured against the
+    # sustained bf16 figure, one that ran at full clock against the burst figure
+    sys.path.insert(0, ROOT)
+    import bench
+    peaks = {"hbm_gbs": 6486.1, "bf16_tflops": 1768.2, "bf16_tflops_sustained": 1385.5}
+    assert bench.tensor_peak(peaks, {"reasons": ["sw_power_cap"]})[0] == 1385.5
+    assert bench.tensor_peak(peaks, {"reasons": []})[0] == 1768.2
+    assert bench.tensor_peak(peaks, None)[0] == 1768.2
+    assert bench.tensor_peak({"hbm_gbs": 1.0, "bf16_tflops": 2.0},
+                             {"reasons": ["sw_power_cap"]})[0] == 2.0
