@@ -177,6 +177,16 @@ SMALL = [
     MoEConfig("bf16_pair_drops", 4096, 128, 4, 2, 128, 1.02, "bf16", seed=14, zipf_bias=True),
     # 512 expected rows per expert, no bias: GEMM1 on CTA pairs, GEMM2 on single CTAs
     MoEConfig("bf16_mixed_tiles_t2048", 2048, 256, 8, 2, 384, 1.25, "bf16", seed=15),
+    # the smallest batch on the fused routing kernel: 32 tiles, the last one 1 token
+    MoEConfig("bf16_fused_t3969_last_tile_1", 3969, 128, 16, 2, 128, 1.25, "bf16", seed=16),
+    # a long hidden size: the router splits K 16 ways, GEMM1 runs 128 k-chunks
+    MoEConfig("bf16_h8192", 256, 8192, 8, 2, 128, None, "bf16", seed=17),
+    # a wide expert: GEMM2 runs 256 k-chunks
+    MoEConfig("bf16_f16384", 512, 128, 2, 1, 16384, 1.5, "bf16", seed=18),
+    # 256 experts, top-1, on the fused routing kernel: ~16 rows per expert
+    MoEConfig("bf16_fused_n256_k1", 4096, 128, 256, 1, 64, 2.0, "bf16", seed=19),
+    # k = N in bf16 on the fused routing kernel: every token visits every expert
+    MoEConfig("bf16_fused_dense_k8", 4096, 128, 8, 8, 64, None, "bf16", seed=20),
 ]
 
 
