@@ -214,16 +214,19 @@ void choose_tiles(Plan& p, bool has_bias) {
 }
 
 int device_check() {
-  static int ok_dev[64] = {0};  // 0 unknown, 1 sm_103, -1 other
+  static std::atomic<int> ok_dev[64];  // 0 unknown, 1 sm_103, -1 other
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ECUDA;
-  if (dev >= 0 && dev < 64 && ok_dev[dev] != 0) return ok_dev[dev] > 0 ? MOE_OK : MOE_ENODEVICE;
+  if (dev >= 0 && dev < 64) {
+    const int known = ok_dev[dev].load(std::memory_order_relaxed);
+    if (known != 0) return known > 0 ? MOE_OK : MOE_ENODEVICE;
+  }
   int major = 0, minor = 0;
   if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
     return MOE_ECUDA;
   const bool ok = major == 10 && minor == 3;
-  if (dev >= 0 && dev < 64) ok_dev[dev] = ok ? 1 : -1;
+  if (dev >= 0 && dev < 64) ok_dev[dev].store(ok ? 1 : -1, std::memory_order_relaxed);
   return ok ? MOE_OK : MOE_ENODEVICE;
 }
 
