@@ -581,6 +581,7 @@ def measure_workload(cfg, args, device, stream, flush, rank, world, peaks, peak_
     clock = sampler.stop(window) if sampler is not None else None
     kept_slots = int(wl.routing.kept_counts.sum().item())
     touched = int((wl.routing.kept_counts > 0).sum().item())
+    routing = routing_stats(cfg, wl.routing)
     mean_ms = reduce_max(float(step_ms.mean()), world, device)
     total_tokens = reduce_sum(cfg.T, world, device)
     stage_ms = staged_pass(wl, min(args.steps, 200), stream, flush, device)
@@ -590,7 +591,7 @@ def measure_workload(cfg, args, device, stream, flush, rank, world, peaks, peak_
     rec = {"value": round(total_tokens / (mean_ms / 1e3), 1), "ms_per_step": round(mean_ms, 5),
            "step_ms": step_stats(step_ms), "kept_slots": kept_slots, "touched_experts": touched,
            "global_tokens": int(total_tokens), "grouped_gemm": grouped, "kernels": per_kernel,
-           "staged_ms_per_step": staged, "roofline": roofline,
+           "staged_ms_per_step": staged, "roofline": roofline, "routing": routing,
            "gpu_launches": launches_per_forward(cfg) * args.steps,
            "plan": moe.describe(wl.c, has_bias=wl.dev.router_bias is not None),
            "wall_s_timed_region": round(window[1] - window[0], 3)}
@@ -602,6 +603,23 @@ def measure_workload(cfg, args, device, stream, flush, rank, world, peaks, peak_
     torch.cuda.synchronize(device)
     torch.cuda.empty_cache()
     return rec
+
+
+def routing_stats(cfg, routing) -> dict:
+    """Expert utilisation of the last timed forward, from the layer's own outputs: the
+    aux loss, slots dropped by capacity, rows per expert (before and after capacity)
+    and their imbalance (coefficient of variation of the routed counts)."""
+    counts = routing.expert_counts.double()
+    kept = routing.kept_counts
+    mean = float(counts.mean()) if counts.numel() else 0.0
+    cv = float(counts.std(unbiased=False)) / mean if mean > 0 else 0.0
+    return {"aux_loss": round(float(routing.aux_loss.item()), 6),
+            "dropped_slots": int(counts.sum().item() - kept.sum().item()),
+            "routed_rows_max": int(counts.max().item()) if counts.numel() else 0,
+            "routed_rows_min": int(counts.min().item()) if counts.numel() else 0,
+            "kept_rows_max": int(kept.max().item()) if kept.numel() else 0,
+            "load_cv": round(cv, 4),
+            "active_fraction": round(cfg.k / cfg.N, 6)}
 
 
 def cfg_record(cfg, world: int) -> dict:

@@ -179,3 +179,22 @@ def test_tensor_peak_follows_the_power_regime_of_the_timed_region():
     assert bench.tensor_peak(peaks, None)[0] == 1768.2
     assert bench.tensor_peak({"hbm_gbs": 1.0, "bf16_tflops": 2.0},
                              {"reasons": ["sw_power_cap"]})[0] == 2.0
+
+
+def test_routing_stats_from_the_layer_outputs():
+    # utilisation figures the bench prints, computed from routing outputs alone
+    import types
+
+    import torch
+    sys.path.insert(0, ROOT)
+    import bench
+    from mixture_experts_layer_102_b300 import configs
+    cfg = configs.TINY_F32.with_(N=4, k=2)
+    r = types.SimpleNamespace(expert_counts=torch.tensor([60, 30, 20, 18], dtype=torch.int32),
+                              kept_counts=torch.tensor([40, 30, 20, 18], dtype=torch.int32),
+                              aux_loss=torch.tensor([1.25]))
+    d = bench.routing_stats(cfg, r)
+    assert d["dropped_slots"] == 20 and d["routed_rows_max"] == 60 and d["routed_rows_min"] == 18
+    assert d["kept_rows_max"] == 40 and d["active_fraction"] == 0.5 and d["aux_loss"] == 1.25
+    c = torch.tensor([60., 30., 20., 18.])
+    assert abs(d["load_cv"] - float(c.std(unbiased=False) / c.mean())) < 1e-4
