@@ -60,9 +60,11 @@ combine_kernel(const TIo* __restrict__ ye, const int32_t* __restrict__ slot_row,
 #pragma unroll
         for (int u = 0; u < VPL; ++u) {
           const int g = g0 + u * 32 + lane;
-          if (g < ngrp)
+          if (g < ngrp) {
+            const uint4* v = reinterpret_cast<const uint4*>(src + g * 8);
 #pragma unroll
-            for (int i = 0; i < N16; ++i) raw[j][u][i] = reinterpret_cast<const uint4*>(src + g * 8)[i];
+            for (int i = 0; i < N16; ++i) raw[j][u][i] = v[i];
+          }
         }
       }
 #pragma unroll
@@ -75,16 +77,16 @@ combine_kernel(const TIo* __restrict__ ye, const int32_t* __restrict__ slot_row,
           const int g = g0 + u * 32 + lane;
           if (g < ngrp) {
             if constexpr (sizeof(TIo) == 2) {
-              const uint32_t v[4] = {raw[j][u][0].x, raw[j][u][0].y, raw[j][u][0].z, raw[j][u][0].w};
+              const uint4 x = raw[j][u][0];
+              const uint32_t v[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
               for (int q = 0; q < 4; ++q) {
                 acc[u][2 * q] = fmaf(ws, bf16_lo(v[q]), acc[u][2 * q]);
                 acc[u][2 * q + 1] = fmaf(ws, bf16_hi(v[q]), acc[u][2 * q + 1]);
               }
             } else {
-              const uint32_t v[8] = {raw[j][u][0].x, raw[j][u][0].y, raw[j][u][0].z, raw[j][u][0].w,
-                                     raw[j][u][N16 - 1].x, raw[j][u][N16 - 1].y,
-                                     raw[j][u][N16 - 1].z, raw[j][u][N16 - 1].w};
+              const uint4 x = raw[j][u][0], y = raw[j][u][N16 - 1];
+              const uint32_t v[8] = {x.x, x.y, x.z, x.w, y.x, y.y, y.z, y.w};
 #pragma unroll
               for (int q = 0; q < 8; ++q) acc[u][q] = fmaf(ws, __uint_as_float(v[q]), acc[u][q]);
             }
