@@ -177,12 +177,12 @@ int moe_get_status(void* workspace, size_t workspace_bytes, void* stream,
  * scratch does not fit that array (roughly: ksplit*T*N*4 partial logits plus about
  * 16*T*k bytes; every named workload here fits). The first call on a device looks
  * up the array's device address (cudaGetSymbolAddress) with that device current and
- * keeps it for the life of the process; make that first call before any stream
- * capture, and do not use this call on a device after cudaDeviceReset() on it (the
- * kept address would be stale). All calls share the array and it keeps the last
- * call's contents: calls that overlap on the GPU (other streams, other threads) race
- * and must be serialised by the caller. Each call clears the array's status word
- * before its kernels run; moe_get_status_static() reads what they reported.
+ * keeps it for the life of the process; do not use this call on a device after
+ * cudaDeviceReset() on it (the kept address would be stale). All calls share the
+ * array and it keeps the last call's contents: calls that overlap on the GPU (other
+ * streams, other threads) race and must be serialised by the caller. Each call clears
+ * the array's status word before its kernels run; moe_get_status_static() reads what
+ * they reported.
  */
 #define MOE_STATIC_SCRATCH_BYTES ((size_t)16 << 20)
 
