@@ -255,5 +255,101 @@ __device__ inline void finish_routing(const SelectArgs& a, int nblk) {
   layout_experts(s_kept, Ntot, lay);
 }
 
+// The same finish for small layers in one warp, with no block barrier: at most 32
+// routed experts, at most MAXR * (32 / np2(N)) blocks, no mask and neither optional
+// loss. L = 32 / np2(N) lanes share an expert column, each summing a contiguous range
+// of at most MAXR block rows held in registers; a prefix over those ranges (shuffles)
+// gives every block its base. Lane e < N ends up with expert e's totals, so the aux
+// sum reduces the same per-expert products as the block version.
+// The kernels take the finish as a template argument chosen on the host, so each
+// carries the code of one finish only.
+template <int MAXR>
+inline bool warp_finish_fits(const SelectArgs& a, int nblk) {
+  if (a.valid != nullptr || a.aux_kl != nullptr || a.aux_std2 != nullptr || a.N > 32)
+    return false;
+  int np2 = 1;
+  while (np2 < a.N) np2 <<= 1;
+  return nblk <= MAXR * (32 / np2);
+}
+
+// Called by warp 0 only, where warp_finish_fits<MAXR>() holds.
+template <int MAXR>
+__device__ inline void finish_routing_warp(const SelectArgs& a, int nblk) {
+  __shared__ int32_t s_rows[32 + MAX_SHARED];
+  const unsigned FULL = 0xffffffffu;
+  const int lane = threadIdx.x;
+  const int N = a.N, Ntot = a.N + a.S;
+  int np2 = 1;
+  while (np2 < N) np2 <<= 1;
+  const int L = 32 / np2;                       // lanes per expert column
+  const int col = lane % np2, part = lane / np2;
+  const int R = (nblk + L - 1) / L;             // <= MAXR
+  const int r0 = min(nblk, part * R), r1 = min(nblk, r0 + R);
+  const bool mine = col < N;
+  int c[MAXR];
+  float p[MAXR];
+#pragma unroll
+  for (int u = 0; u < MAXR; ++u) {
+    const bool in = mine && r0 + u < r1;
+    c[u] = in ? a.blk_counts[(size_t)(r0 + u) * N + col] : 0;
+    p[u] = in ? a.blk_psum[(size_t)(r0 + u) * N + col] : 0.f;
+  }
+  int isum = 0;
+  float fsum = 0.f;
+#pragma unroll
+  for (int u = 0; u < MAXR; ++u) {
+    isum += c[u];
+    fsum += p[u];
+  }
+  int before = 0, total = 0;  // the column's slots in earlier ranges, and in all
+  float ftot = 0.f;
+  for (int q = 0; q < L; ++q) {
+    const int v = __shfl_sync(FULL, isum, col + q * np2);
+    const float fv = __shfl_sync(FULL, fsum, col + q * np2);
+    if (q < part) before += v;
+    total += v;
+    ftot += fv;
+  }
+  if (mine) {  // exclusive per-expert base of every block
+    int run = before;
+#pragma unroll
+    for (int u = 0; u < MAXR; ++u) {
+      if (r0 + u < r1) a.blk_counts[(size_t)(r0 + u) * N + col] = run;
+      run += c[u];
+    }
+  }
+  const long long C = a.C;
+  const int kept = (C < 0 || (long long)total <= C) ? total : (int)C;
+  if (mine && part == 0) {
+    s_rows[col] = kept;
+    a.counts[col] = total;
+    a.kept[col] = kept;
+    if (a.user_counts != nullptr) a.user_counts[col] = total;
+    if (a.user_kept != nullptr) a.user_kept[col] = kept;
+  }
+  for (int j = lane; j < a.S; j += 32) {  // shared experts take every token
+    s_rows[N + j] = a.T;
+    a.counts[N + j] = a.T;
+    a.kept[N + j] = a.T;
+  }
+  // aux = N * sum_e (counts_e / (T*k)) * (Psum_e / T), as in finish_routing
+  float fp = (mine && part == 0) ? (float)total * ftot : 0.f;
+#pragma unroll
+  for (int d = 16; d > 0; d >>= 1) fp += __shfl_xor_sync(FULL, fp, d);
+  if (lane == 0) {
+    *a.cap = (int32_t)C;
+    const float Tf = (float)a.T;
+    *a.aux = a.T > 0 ? (float)N * (fp / (Tf * (float)a.k)) / Tf : 0.f;
+  }
+  __syncwarp();
+  ExpertLayout lay;
+  lay.offsets = a.offsets;
+  for (int tb = 0; tb < 2; ++tb) {
+    lay.tile_first[tb] = a.tile_first[tb];
+    lay.num_mtiles[tb] = a.num_mtiles[tb];
+  }
+  layout_experts(s_rows, Ntot, lay);
+}
+
 }  // namespace route
 }  // namespace moe

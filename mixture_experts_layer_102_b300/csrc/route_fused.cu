@@ -46,6 +46,7 @@ constexpr int TOK = 128;                        // tokens per CTA (TMEM lanes)
 constexpr uint32_t A_BYTES = TOK * BK * 2;      // 16 KB
 constexpr int NUM_THREADS = 256;
 constexpr int MAX_STAGES = 16;
+constexpr int WARP_FINISH_ROWS = 16;            // block rows per lane in the one-warp finish
 
 // Row stride (floats) of the tile's logits in shared memory: at least N + 1 and 2 mod 4,
 // so the two threads of each of a warp's 16 tokens (experts of one parity each) fall
@@ -63,6 +64,8 @@ struct FusedArgs {
   uint32_t* status;
 };
 
+// WF: the finish runs in one warp (finish_routing_warp), else in the whole CTA.
+template <bool WF>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 route_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                    FusedArgs f) {
@@ -375,7 +378,11 @@ route_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
   __syncthreads();
   if (!is_last) return;
   __threadfence();
-  finish_routing(a, gridDim.x);
+  if constexpr (WF) {
+    if (threadIdx.x < 32) finish_routing_warp<WARP_FINISH_ROWS>(a, gridDim.x);
+  } else {
+    finish_routing(a, gridDim.x);
+  }
   if (threadIdx.x == 0) *a.done = 0u;  // ready for the next call
 }
 
@@ -398,24 +405,28 @@ cudaError_t launch_route_fused(const SelectArgs& s, const void* x, const void* w
   // kind::f16 descriptor: D fp32, A/B bf16, K-major, N = n_pad, M = 128
   f.idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(f.n_pad >> 3) << 17) |
             ((uint32_t)(TOK >> 4) << 24);
+  const int nblk = (s.T + TOK - 1) / TOK;
+  const bool wf = route::warp_finish_fits<WARP_FINISH_ROWS>(s, nblk);
+  auto kernel = wf ? route_fused_kernel<true> : route_fused_kernel<false>;
   // the kernel's static shared memory (once per process: it does not depend on the
   // device) and the device's opt-in limit bound the dynamic part
-  static size_t static_smem = 0;
-  static std::once_flag once;
+  static size_t static_smem[2] = {0, 0};
+  static std::once_flag once[2];
   cudaError_t e = cudaSuccess;
-  std::call_once(once, [&] {
+  std::call_once(once[wf ? 1 : 0], [&] {
     cudaFuncAttributes attr;
-    e = cudaFuncGetAttributes(&attr, route_fused_kernel);
-    static_smem = attr.sharedSizeBytes;
+    e = cudaFuncGetAttributes(&attr, kernel);
+    static_smem[wf ? 1 : 0] = attr.sharedSizeBytes;
   });
-  if (e != cudaSuccess || static_smem == 0) return e != cudaSuccess ? e : cudaErrorInvalidValue;
+  const size_t kstatic = static_smem[wf ? 1 : 0];
+  if (e != cudaSuccess || kstatic == 0) return e != cudaSuccess ? e : cudaErrorInvalidValue;
   size_t optin = 0;
   e = smem_optin_bytes(&optin);
   if (e != cudaSuccess) return e;
   const size_t epi = (size_t)TOK * logit_stride(s.N) * 4 + (size_t)TOK * s.k * 4 + (size_t)TOK * s.N;
   const size_t tail = 8 * (2 * MAX_STAGES + 1) + 16;  // barriers, TMEM address, abort flag
-  if (optin < static_smem + 1024 + tail) return cudaErrorInvalidValue;
-  const size_t avail = optin - static_smem - 1024 - tail;
+  if (optin < kstatic + 1024 + tail) return cudaErrorInvalidValue;
+  const size_t avail = optin - kstatic - 1024 - tail;
   int stages = (int)(avail / f.stage_bytes);
   if (stages > MAX_STAGES) stages = MAX_STAGES;
   if (stages > f.kc_total) stages = f.kc_total > 1 ? f.kc_total : 1;
@@ -430,9 +441,9 @@ cudaError_t launch_route_fused(const SelectArgs& s, const void* x, const void* w
   if (!make_map(&mX, x, 2, (uint64_t)H, 0, (uint64_t)s.T, TOK)) return cudaErrorInvalidValue;
   if (!make_map(&mW, w_router, 2, (uint64_t)H, 0, (uint64_t)s.N, (uint32_t)f.n_pad))
     return cudaErrorInvalidValue;
-  e = ensure_dynamic_smem(reinterpret_cast<const void*>(route_fused_kernel), smem);
+  e = ensure_dynamic_smem(reinterpret_cast<const void*>(kernel), smem);
   if (e != cudaSuccess) return e;
-  return launch_kernel(route_fused_kernel, dim3((s.T + TOK - 1) / TOK), dim3(NUM_THREADS), smem,
+  return launch_kernel(kernel, dim3(nblk), dim3(NUM_THREADS), smem,
                        stream, pdl, mX, mW, f);
 }
 

@@ -52,10 +52,12 @@ using namespace route;
 
 constexpr int WARPS = SELECT_WARPS;  // 32
 constexpr int MAX_TPW = 4;           // tokens per warp whose ranks stay in registers
+constexpr int WARP_FINISH_ROWS = 8;  // block rows per lane in the one-warp finish
 
 // OPT: the valid-token mask or the variance loss may be in use (read at run time);
 // without it those branches are compiled out of the base layer's kernel.
-template <bool OPT>
+// WF: the finish runs in one warp (finish_routing_warp), else in the whole block.
+template <bool OPT, bool WF>
 __global__ void __launch_bounds__(1024) route_select_kernel(SelectArgs a) {
   extern __shared__ int32_t dyn[];
   int32_t* cnt = dyn;                                   // [WARPS][N] running counts
@@ -264,7 +266,11 @@ __global__ void __launch_bounds__(1024) route_select_kernel(SelectArgs a) {
   __syncthreads();
   if (!is_last) return;
   __threadfence();
-  finish_routing(a, gridDim.x);
+  if constexpr (WF) {
+    if (threadIdx.x < 32) finish_routing_warp<WARP_FINISH_ROWS>(a, gridDim.x);
+  } else {
+    finish_routing(a, gridDim.x);
+  }
   if (threadIdx.x == 0) *a.done = 0u;  // ready for the next call
 }
 
@@ -274,7 +280,11 @@ cudaError_t launch_route_select(const SelectArgs& a, int nblk, cudaStream_t stre
   if (a.T == 0) return cudaSuccess;
   const size_t smem = (size_t)WARPS * a.N * 8;  // counters and P sums of every warp
   const bool opt = a.valid != nullptr || a.aux_std2 != nullptr;
-  auto kernel = opt ? route_select_kernel<true> : route_select_kernel<false>;
+  // options that need the block finish (a mask, the variance loss) exclude the warp one
+  auto kernel = opt ? route_select_kernel<true, false>
+                : route::warp_finish_fits<WARP_FINISH_ROWS>(a, nblk)
+                    ? route_select_kernel<false, true>
+                    : route_select_kernel<false, false>;
   const cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(kernel), smem);
   if (e != cudaSuccess) return e;
   return launch_kernel(kernel, dim3(nblk), dim3(WARPS * 32), smem, stream, pdl, a);

@@ -184,6 +184,10 @@ CASES = [
                seed=50, zipf_bias=True), 1, "swiglu", 500),
     (MoEConfig("bf16_fused_n1_k1_t4096", 4096, 128, 1, 1, 64, None, "bf16", seed=39), 0,
      "swiglu", None),
+    # one-warp routing finish: 4 lanes per expert column over ragged ranges of the 40
+    # blocks, with shared experts and capacity drops
+    (MoEConfig("bf16_fused_n5_t5000_warp_finish", 5000, 128, 5, 2, 64, 1.1, "bf16", seed=52,
+               zipf_bias=True), 2, "swiglu", None),
     (MoEConfig("bf16_fused_k32_n64_masked_shared", 4100, 64, 64, 32, 64, 0.9, "bf16", seed=40,
                zipf_bias=True), 2, "gelu", 300),
     (configs.TINY_F32.with_(name="f32_shared2_tight", capacity_factor=0.6), 2, "swiglu", None),

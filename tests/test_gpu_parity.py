@@ -187,6 +187,9 @@ SMALL = [
     MoEConfig("bf16_fused_n256_k1", 4096, 128, 256, 1, 64, 2.0, "bf16", seed=19),
     # k = N in bf16 on the fused routing kernel: every token visits every expert
     MoEConfig("bf16_fused_dense_k8", 4096, 128, 8, 8, 64, None, "bf16", seed=20),
+    # the two-launch routing path's one-warp finish: 22 blocks of 32 tokens in ragged
+    # ranges of 4 lanes per expert column
+    MoEConfig("bf16_select_n6_t700_warp_finish", 700, 128, 6, 2, 128, 1.1, "bf16", seed=21),
 ]
 
 
