@@ -9,8 +9,8 @@
 //   the routing-decision kernel (route_select.cu), whose outputs this kernel writes in
 //   the same form with a block of 128 tokens.
 //
-// One CTA per 128-token tile, 256 threads, no split of K, so the logits never leave
-// the CTA as partial sums:
+// One CTA per 128-token tile, 256 threads (512 above 32 experts), no split of K, so
+// the logits never leave the CTA as partial sums:
 //   warp 0      TMA producer: x rows and W_r ([N, H], N_pad = N rounded up to 16 rows,
 //               zero past N) stream through as many 128-byte-swizzled stages as shared
 //               memory holds, so the load pipeline covers HBM latency.
@@ -18,7 +18,7 @@
 //               N=N_pad, K=16) into a TMEM accumulator.
 //   warps 2-5   read the accumulator back (one token per thread: the TMEM lane) and
 //               stage the logits (+ bias) in the freed stage memory.
-//   all warps   two threads per token (experts of one parity each, combined by
+//   all warps   two (four) threads per token (experts e = h mod 2 (4) each, combined by
 //               shuffles) make the token's decisions: softmax by max and sum, the top k
 //               by k passes, each taking the best logit strictly after the previous
 //               pick in the order (logit descending, id ascending), the gate weights,
@@ -44,15 +44,15 @@ using namespace route;
 constexpr int BK = 64;                          // 64 bf16 = one 128-byte swizzle row
 constexpr int TOK = 128;                        // tokens per CTA (TMEM lanes)
 constexpr uint32_t A_BYTES = TOK * BK * 2;      // 16 KB
-constexpr int NUM_THREADS = 256;
 constexpr int MAX_STAGES = 16;
 constexpr int WARP_FINISH_ROWS = 16;            // block rows per lane in the one-warp finish
 
-// Row stride (floats) of the tile's logits in shared memory: at least N + 1 and 2 mod 4,
-// so the two threads of each of a warp's 16 tokens (experts of one parity each) fall
-// in 32 different banks.
-__host__ __device__ constexpr int logit_stride(int N) {
-  return (N + 1) % 4 == 2 ? N + 1 : (N + 2) % 4 == 2 ? N + 2 : (N + 3) % 4 == 2 ? N + 3 : N + 4;
+// Row stride (floats) of the tile's logits in shared memory: at least N + 1 and an odd
+// multiple of tpt (the threads per token), so the tpt threads of each of a warp's
+// 32/tpt tokens (experts e = h mod tpt each) fall in 32 different banks.
+__host__ __device__ constexpr int logit_stride(int N, int tpt) {
+  return ((N + 1 + tpt - 1) / tpt) % 2 == 1 ? (N + 1 + tpt - 1) / tpt * tpt
+                                             : ((N + 1 + tpt - 1) / tpt + 1) * tpt;
 }
 
 struct FusedArgs {
@@ -65,10 +65,12 @@ struct FusedArgs {
 };
 
 // WF: the finish runs in one warp (finish_routing_warp), else in the whole CTA.
-template <bool WF>
+// NUM_THREADS: 256 (two threads per token in the decisions) or 512 (four).
+template <bool WF, int NUM_THREADS>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 route_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                    FusedArgs f) {
+  constexpr int TPT = NUM_THREADS / TOK;  // threads per token in the decisions
   const SelectArgs& a = f.s;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -178,10 +180,10 @@ route_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
   }
   // Epilogue shared memory, in the stage region (every load has landed and every MMA
   // has read its operands once the accumulator barrier flips):
-  //   L  [TOK][LS]  logits, then probabilities     (fp32, LS = logit_stride(N))
+  //   L  [TOK][LS]  logits, then probabilities     (fp32, LS = logit_stride(N, TPT))
   //   SEL[TOK][k]   the selected experts            (int32)
   //   CH [TOK][N]   slot + 1 of a selected expert   (bytes, 0 = not selected)
-  const int LS = logit_stride(N);
+  const int LS = logit_stride(N, TPT);
   float* L = reinterpret_cast<float*>(base_ptr);
   int32_t* SEL = reinterpret_cast<int32_t*>(base_ptr + (size_t)TOK * LS * 4);
   uint8_t* CH = base_ptr + (size_t)TOK * LS * 4 + (size_t)TOK * k * 4;
@@ -223,10 +225,10 @@ route_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
                  "r"(f.tmem_cols)
                  : "memory");
   }
-  // ------------------------------------------- per-token decisions (all 8 warps)
-  // Two threads per token, adjacent lanes: thread h of token r takes the experts of
-  // parity h. Every thread runs the picks and the sum (so the pair's shuffles are
-  // never divergent); only live tokens write. Any timeout (abort flag) leaves every
+  // ------------------------------------------------- per-token decisions (all warps)
+  // TPT threads per token, adjacent lanes: thread h of token r takes the experts
+  // e = h mod TPT. Every thread runs the picks and the sum (so the shuffles are never
+  // divergent); only live tokens write. Any timeout (abort flag) leaves every
   // token of the tile without a decision, as padding. Passes over the token's experts:
   // k picks (the first also clears the selection marks, and its value is the row's
   // maximum), then one pass that turns each logit into exp(l - max), summing them.
@@ -237,7 +239,7 @@ route_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
   float d2 = 0.f;
   {
     const unsigned FULL = 0xffffffffu;
-    const int r = threadIdx.x >> 1, h = threadIdx.x & 1;
+    const int r = threadIdx.x / TPT, h = threadIdx.x % TPT;
     const int t = m0 + r;
     float* row = L + r * LS;
     uint8_t* ch = CH + (size_t)r * N;
@@ -245,14 +247,14 @@ route_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
     const bool live = *abort_flag == 0 && t < a.T && (!masked || a.valid[t] != 0);
     if (h == 0) s_valid[r] = live ? 1 : 0;
     // top k: pick j is the best logit strictly after pick j-1 in (logit desc, id asc);
-    // each thread scans its parity, and the pair keeps the better of its two candidates
+    // each thread scans its experts, and the token's threads keep the best candidate
     float pl = INFINITY, l0 = 0.f, zs = 0.f, m = -INFINITY;
     int pi = -1;
     for (int j = 0; j < k; ++j) {
       float bv = -INFINITY;
       int bi = -1;
 #pragma unroll 8
-      for (int e = h; e < N; e += 2) {
+      for (int e = h; e < N; e += TPT) {
         const float v = row[e];
         if (j == 0) ch[e] = 0;
         const bool after = v < pl || (v == pl && e > pi);
@@ -261,33 +263,36 @@ route_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
           bi = e;
         }
       }
-      const float ov = __shfl_xor_sync(FULL, bv, 1);
-      const int oi = __shfl_xor_sync(FULL, bi, 1);
-      if (oi >= 0 && (bi < 0 || ov > bv || (ov == bv && oi < bi))) {
-        bv = ov;
-        bi = oi;
+#pragma unroll
+      for (int o = 1; o < TPT; o <<= 1) {  // the token's threads keep the best candidate
+        const float ov = __shfl_xor_sync(FULL, bv, o);
+        const int oi = __shfl_xor_sync(FULL, bi, o);
+        if (oi >= 0 && (bi < 0 || ov > bv || (ov == bv && oi < bi))) {
+          bv = ov;
+          bi = oi;
+        }
       }
       if (j == 0 && bi >= 0) m = bv;  // the largest logit of the row
       if (bi < 0) {  // only NaN logits leave no candidate: keep the index in range
         bi = j;
         bv = row[j];
       }
-      if ((j & 1) == h) sel[j] = bi;
+      if (j % TPT == h) sel[j] = bi;
       if (j == 0) l0 = bv;
       zs += expf(bv - l0);
       pl = bv;
       pi = bi;
     }
-    __syncwarp();  // the pair's picks and cleared marks are in place
+    __syncwarp();  // the token's picks and cleared marks are in place
     if (live) {
-      for (int j = h; j < k; j += 2) {  // gate weights: softmax over the k selected logits
+      for (int j = h; j < k; j += TPT) {  // gate weights: softmax over the k selected logits
         const int e = sel[j];
         a.idx[(size_t)t * k + j] = e;
         a.w[(size_t)t * k + j] = expf(row[e] - l0) / zs;
         ch[e] = (uint8_t)(j + 1);
       }
     } else if (t < a.T) {  // padding: no expert, weight 0
-      for (int j = h; j < k; j += 2) {
+      for (int j = h; j < k; j += TPT) {
         a.idx[(size_t)t * k + j] = -1;
         a.w[(size_t)t * k + j] = 0.f;
       }
@@ -295,18 +300,19 @@ route_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
     __syncwarp();  // the gates have read the logits they need
     float sum = 0.f;
 #pragma unroll 8
-    for (int e = h; e < N; e += 2) {  // exp(l - max) replaces each logit
+    for (int e = h; e < N; e += TPT) {  // exp(l - max) replaces each logit
       const float x = live ? expf(row[e] - m) : 0.f;
       row[e] = x;
       sum += x;
     }
-    sum += __shfl_xor_sync(FULL, sum, 1);  // the same sum on both threads
+#pragma unroll
+    for (int o = 1; o < TPT; o <<= 1) sum += __shfl_xor_sync(FULL, sum, o);  // same on all
     const float inv = 1.f / sum;
     if (h == 0) s_inv[r] = live ? inv : 0.f;
     if (want_d2 && live) {
       const float invN = 1.f / (float)N;
 #pragma unroll 8
-      for (int e = h; e < N; e += 2) {
+      for (int e = h; e < N; e += TPT) {
         const float pe = __fmul_rn(row[e], inv);
         d2 = fmaf(pe - invN, pe - invN, d2);
       }
@@ -406,24 +412,32 @@ cudaError_t launch_route_fused(const SelectArgs& s, const void* x, const void* w
   f.idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(f.n_pad >> 3) << 17) |
             ((uint32_t)(TOK >> 4) << 24);
   const int nblk = (s.T + TOK - 1) / TOK;
+  // Above 32 experts the decisions and the column pass take four threads per token
+  // (same-call A/B on the fine-grained layer: route stage 48.5 -> 45.1 us); the
+  // smaller layers were no faster with them. The one-warp finish needs N <= 32.
   const bool wf = route::warp_finish_fits<WARP_FINISH_ROWS>(s, nblk);
-  auto kernel = wf ? route_fused_kernel<true> : route_fused_kernel<false>;
+  const int variant = wf ? 0 : s.N > 32 ? 2 : 1;
+  const int nthreads = variant == 2 ? 512 : 256;
+  auto kernel = variant == 0 ? route_fused_kernel<true, 256>
+              : variant == 1 ? route_fused_kernel<false, 256>
+                             : route_fused_kernel<false, 512>;
   // the kernel's static shared memory (once per process: it does not depend on the
   // device) and the device's opt-in limit bound the dynamic part
-  static size_t static_smem[2] = {0, 0};
-  static std::once_flag once[2];
+  static size_t static_smem[3] = {0, 0, 0};
+  static std::once_flag once[3];
   cudaError_t e = cudaSuccess;
-  std::call_once(once[wf ? 1 : 0], [&] {
+  std::call_once(once[variant], [&] {
     cudaFuncAttributes attr;
     e = cudaFuncGetAttributes(&attr, kernel);
-    static_smem[wf ? 1 : 0] = attr.sharedSizeBytes;
+    static_smem[variant] = attr.sharedSizeBytes;
   });
-  const size_t kstatic = static_smem[wf ? 1 : 0];
+  const size_t kstatic = static_smem[variant];
   if (e != cudaSuccess || kstatic == 0) return e != cudaSuccess ? e : cudaErrorInvalidValue;
   size_t optin = 0;
   e = smem_optin_bytes(&optin);
   if (e != cudaSuccess) return e;
-  const size_t epi = (size_t)TOK * logit_stride(s.N) * 4 + (size_t)TOK * s.k * 4 + (size_t)TOK * s.N;
+  const size_t epi = (size_t)TOK * logit_stride(s.N, nthreads / TOK) * 4 +
+                     (size_t)TOK * s.k * 4 + (size_t)TOK * s.N;
   const size_t tail = 8 * (2 * MAX_STAGES + 1) + 16;  // barriers, TMEM address, abort flag
   if (optin < kstatic + 1024 + tail) return cudaErrorInvalidValue;
   const size_t avail = optin - kstatic - 1024 - tail;
@@ -443,8 +457,7 @@ cudaError_t launch_route_fused(const SelectArgs& s, const void* x, const void* w
     return cudaErrorInvalidValue;
   e = ensure_dynamic_smem(reinterpret_cast<const void*>(kernel), smem);
   if (e != cudaSuccess) return e;
-  return launch_kernel(kernel, dim3(nblk), dim3(NUM_THREADS), smem,
-                       stream, pdl, mX, mW, f);
+  return launch_kernel(kernel, dim3(nblk), dim3(nthreads), smem, stream, pdl, mX, mW, f);
 }
 
 }  // namespace moe
