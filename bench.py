@@ -14,8 +14,9 @@ A second pass of forwards through `moe_forward_timed` (an event between every tw
 stages) gives each kernel's time for the roofline. The other named bf16 workloads
 (the 16-expert T=4096 layer, the fine-grained Zipf-skewed layer and the decode-size
 layer) are timed the same way in the same process, before the headline (whose
-seconds-long loop runs at the GPU's power cap), and reported under `other_workloads`,
-each with its own clock record.
+seconds-long loop runs at the GPU's power cap), with at least 300 timed forwards after
+20 warm-up ones, and reported under `other_workloads`, each with its own clock record
+and step counts.
 
 Under torchrun (N > 1) every rank holds all experts and runs its own independent
 batch of T tokens (the same weights, activations drawn from a per-rank seed): the
@@ -53,6 +54,7 @@ E2E_BUFFERS = 3
 DEFAULT_CONFIG = configs.MIXTRAL_T8192
 # timed after the headline workload in the same process (one GPU only)
 OTHER_WORKLOADS = [configs.BF16_T4096, configs.FINEGRAINED_T16384, configs.DECODE_T64]
+OTHER_MIN_STEPS, OTHER_MIN_WARMUP = 300, 20
 FLUSH_BYTES = 256 << 20
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 STAGES = ["router_logits", "route_select", "dispatch", "gemm1_swiglu", "gemm2", "combine"]
@@ -566,9 +568,12 @@ def time_e2e(wl, args, stream, device, rank: int, world: int, total_tokens: floa
 
 
 def measure_workload(cfg, args, device, stream, flush, rank, world, peaks, peak_src,
-                     clocks=False, e2e=False, keep_host=False):
+                     clocks=False, e2e=False, keep_host=False, steps=None, warmup=None):
     """Time one workload: the timed forwards, the staged pass, optionally the clocks of
-    the timed window and the end-to-end loop. Frees its device memory on return."""
+    the timed window and the end-to-end loop. Frees its device memory on return.
+    `steps` and `warmup` default to the command line's."""
+    steps = args.steps if steps is None else steps
+    warmup = args.warmup if warmup is None else warmup
     import torch
     from mixture_experts_layer_102_b300 import moe
     wl = Workload(cfg, device, rank, keep_host)
@@ -577,14 +582,14 @@ def measure_workload(cfg, args, device, stream, flush, rank, world, peaks, peak_
     if sampler is not None:
         sampler.start()
         time.sleep(0.3)  # the sampler's first readings come before the warm-up
-    step_ms, window = time_steps(wl, args.steps, args.warmup, stream, flush, world, device)
+    step_ms, window = time_steps(wl, steps, warmup, stream, flush, world, device)
     clock = sampler.stop(window) if sampler is not None else None
     kept_slots = int(wl.routing.kept_counts.sum().item())
     touched = int((wl.routing.kept_counts > 0).sum().item())
     routing = routing_stats(cfg, wl.routing)
     mean_ms = reduce_max(float(step_ms.mean()), world, device)
     total_tokens = reduce_sum(cfg.T, world, device)
-    stage_ms = staged_pass(wl, min(args.steps, 200), stream, flush, device)
+    stage_ms = staged_pass(wl, min(steps, 200), stream, flush, device)
     e2e_rec = time_e2e(wl, args, stream, device, rank, world, total_tokens) if e2e else None
     per_kernel, roofline, grouped, staged = kernel_report(cfg, stage_ms, kept_slots, touched,
                                                           peaks, peak_src, clock)
@@ -592,7 +597,8 @@ def measure_workload(cfg, args, device, stream, flush, rank, world, peaks, peak_
            "step_ms": step_stats(step_ms), "kept_slots": kept_slots, "touched_experts": touched,
            "global_tokens": int(total_tokens), "grouped_gemm": grouped, "kernels": per_kernel,
            "staged_ms_per_step": staged, "roofline": roofline, "routing": routing,
-           "gpu_launches": launches_per_forward(cfg) * args.steps,
+           "steps": steps, "warmup": warmup,
+           "gpu_launches": launches_per_forward(cfg) * steps,
            "plan": moe.describe(wl.c, has_bias=wl.dev.router_bias is not None),
            "wall_s_timed_region": round(window[1] - window[0], 3)}
     if clocks:
@@ -641,14 +647,19 @@ def run_gpu_arm(args, cfg):
     peaks, peak_src = load_peaks()
 
     # The other workloads run first: the headline's seconds-long loop holds the GPU at
-    # its power cap, which would carry over into whatever runs right after it.
+    # its power cap, which would carry over into whatever runs right after it. They
+    # take at least OTHER_MIN_STEPS timed forwards after OTHER_MIN_WARMUP warm-up ones
+    # (each record gives its counts): a few warm-up forwards of a 0.15 ms layer end
+    # before the GPU's clocks have settled.
     others = {}
     if world == 1 and not args.no_others:
         for oc in OTHER_WORKLOADS:
             if oc.name == cfg.name:
                 continue
             rec = measure_workload(oc, args, device, stream, flush, rank, world, peaks,
-                                   peak_src, clocks=True)
+                                   peak_src, clocks=True,
+                                   steps=max(args.steps, OTHER_MIN_STEPS),
+                                   warmup=max(args.warmup, OTHER_MIN_WARMUP))
             rec["config"] = cfg_record(oc, world)
             others[oc.name] = rec
     head = measure_workload(cfg, args, device, stream, flush, rank, world, peaks, peak_src,
