@@ -255,77 +255,89 @@ __device__ inline void finish_routing(const SelectArgs& a, int nblk) {
   layout_experts(s_kept, Ntot, lay);
 }
 
-// The same finish for small layers in one warp, with no block barrier: at most 32
-// routed experts, at most MAXR * (32 / np2(N)) blocks, no mask and neither optional
-// loss. L = 32 / np2(N) lanes share an expert column, each summing a contiguous range
-// of at most MAXR block rows held in registers; a prefix over those ranges (shuffles)
-// gives every block its base. Lane e < N ends up with expert e's totals, so the aux
-// sum reduces the same per-expert products as the block version.
+// The same finish for small layers in one warp, with no block barrier: no mask and
+// neither optional loss, and few enough blocks that every lane holds its rows of
+// counts and sums of P in registers (at most MAXR). Up to 32 experts, L = 32 / np2(N)
+// lanes share an expert column, each taking a contiguous range of block rows, and a
+// prefix over those ranges (shuffles) gives every block its base. Above 32 experts a
+// lane takes all rows of experts lane, lane + 32, ... one after another. Lane e then
+// holds expert e's totals (e, e + 32, ... above 32 experts), so the aux sum reduces
+// the same per-expert products in the same order as the block finish.
 // The kernels take the finish as a template argument chosen on the host, so each
 // carries the code of one finish only.
 template <int MAXR>
 inline bool warp_finish_fits(const SelectArgs& a, int nblk) {
-  if (a.valid != nullptr || a.aux_kl != nullptr || a.aux_std2 != nullptr || a.N > 32)
-    return false;
+  if (a.valid != nullptr || a.aux_kl != nullptr || a.aux_std2 != nullptr) return false;
   int np2 = 1;
   while (np2 < a.N) np2 <<= 1;
-  return nblk <= MAXR * (32 / np2);
+  return np2 <= 32 ? nblk <= MAXR * (32 / np2) : nblk <= MAXR;
 }
 
 // Called by warp 0 only, where warp_finish_fits<MAXR>() holds.
 template <int MAXR>
 __device__ inline void finish_routing_warp(const SelectArgs& a, int nblk) {
-  __shared__ int32_t s_rows[32 + MAX_SHARED];
+  __shared__ int32_t s_rows[MAX_EXPERTS];
   const unsigned FULL = 0xffffffffu;
   const int lane = threadIdx.x;
   const int N = a.N, Ntot = a.N + a.S;
   int np2 = 1;
   while (np2 < N) np2 <<= 1;
-  const int L = 32 / np2;                       // lanes per expert column
-  const int col = lane % np2, part = lane / np2;
+  const int L = np2 < 32 ? 32 / np2 : 1;        // lanes per expert column
+  const int CPL = np2 > 32 ? np2 / 32 : 1;      // expert columns per lane
+  const int part = np2 < 32 ? lane / np2 : 0;
   const int R = (nblk + L - 1) / L;             // <= MAXR
   const int r0 = min(nblk, part * R), r1 = min(nblk, r0 + R);
-  const bool mine = col < N;
-  int c[MAXR];
-  float p[MAXR];
-#pragma unroll
-  for (int u = 0; u < MAXR; ++u) {
-    const bool in = mine && r0 + u < r1;
-    c[u] = in ? a.blk_counts[(size_t)(r0 + u) * N + col] : 0;
-    p[u] = in ? a.blk_psum[(size_t)(r0 + u) * N + col] : 0.f;
-  }
-  int isum = 0;
-  float fsum = 0.f;
-#pragma unroll
-  for (int u = 0; u < MAXR; ++u) {
-    isum += c[u];
-    fsum += p[u];
-  }
-  int before = 0, total = 0;  // the column's slots in earlier ranges, and in all
-  float ftot = 0.f;
-  for (int q = 0; q < L; ++q) {
-    const int v = __shfl_sync(FULL, isum, col + q * np2);
-    const float fv = __shfl_sync(FULL, fsum, col + q * np2);
-    if (q < part) before += v;
-    total += v;
-    ftot += fv;
-  }
-  if (mine) {  // exclusive per-expert base of every block
-    int run = before;
+  const long long C = a.C;
+  float fp = 0.f;  // sum over this lane's experts of count * sum of P
+  for (int cc = 0; cc < CPL; ++cc) {
+    const int col = np2 < 32 ? lane % np2 : lane + 32 * cc;
+    const bool mine = col < N;
+    int c[MAXR];
+    float p[MAXR];
 #pragma unroll
     for (int u = 0; u < MAXR; ++u) {
-      if (r0 + u < r1) a.blk_counts[(size_t)(r0 + u) * N + col] = run;
-      run += c[u];
+      const bool in = mine && r0 + u < r1;
+      c[u] = in ? a.blk_counts[(size_t)(r0 + u) * N + col] : 0;
+      p[u] = in ? a.blk_psum[(size_t)(r0 + u) * N + col] : 0.f;
     }
-  }
-  const long long C = a.C;
-  const int kept = (C < 0 || (long long)total <= C) ? total : (int)C;
-  if (mine && part == 0) {
-    s_rows[col] = kept;
-    a.counts[col] = total;
-    a.kept[col] = kept;
-    if (a.user_counts != nullptr) a.user_counts[col] = total;
-    if (a.user_kept != nullptr) a.user_kept[col] = kept;
+    int isum = 0;
+    float fsum = 0.f;
+#pragma unroll
+    for (int u = 0; u < MAXR; ++u) {
+      isum += c[u];
+      fsum += p[u];
+    }
+    int before = 0, total = isum;  // the column's slots in earlier ranges, and in all
+    float ftot = fsum;
+    if (L > 1) {
+      const int base_lane = lane % np2;
+      total = 0;
+      ftot = 0.f;
+      for (int q = 0; q < L; ++q) {
+        const int v = __shfl_sync(FULL, isum, base_lane + q * np2);
+        const float fv = __shfl_sync(FULL, fsum, base_lane + q * np2);
+        if (q < part) before += v;
+        total += v;
+        ftot += fv;
+      }
+    }
+    if (mine) {  // exclusive per-expert base of every block
+      int run = before;
+#pragma unroll
+      for (int u = 0; u < MAXR; ++u) {
+        if (r0 + u < r1) a.blk_counts[(size_t)(r0 + u) * N + col] = run;
+        run += c[u];
+      }
+    }
+    const int kept = (C < 0 || (long long)total <= C) ? total : (int)C;
+    if (mine && part == 0) {
+      s_rows[col] = kept;
+      a.counts[col] = total;
+      a.kept[col] = kept;
+      if (a.user_counts != nullptr) a.user_counts[col] = total;
+      if (a.user_kept != nullptr) a.user_kept[col] = kept;
+      fp = fmaf((float)total, ftot, fp);
+    }
   }
   for (int j = lane; j < a.S; j += 32) {  // shared experts take every token
     s_rows[N + j] = a.T;
@@ -333,7 +345,6 @@ __device__ inline void finish_routing_warp(const SelectArgs& a, int nblk) {
     a.kept[N + j] = a.T;
   }
   // aux = N * sum_e (counts_e / (T*k)) * (Psum_e / T), as in finish_routing
-  float fp = (mine && part == 0) ? (float)total * ftot : 0.f;
 #pragma unroll
   for (int d = 16; d > 0; d >>= 1) fp += __shfl_xor_sync(FULL, fp, d);
   if (lane == 0) {

@@ -414,7 +414,8 @@ cudaError_t launch_route_fused(const SelectArgs& s, const void* x, const void* w
   const int nblk = (s.T + TOK - 1) / TOK;
   // Above 32 experts the decisions and the column pass take four threads per token
   // (same-call A/B on the fine-grained layer: route stage 48.5 -> 45.1 us); the
-  // smaller layers were no faster with them. The one-warp finish needs N <= 32.
+  // smaller layers were no faster with them. With 32 or more blocks the one-warp
+  // finish fits up to 16 experts.
   const bool wf = route::warp_finish_fits<WARP_FINISH_ROWS>(s, nblk);
   const int variant = wf ? 0 : s.N > 32 ? 2 : 1;
   const int nthreads = variant == 2 ? 512 : 256;

@@ -190,6 +190,8 @@ SMALL = [
     # the two-launch routing path's one-warp finish: 22 blocks of 32 tokens in ragged
     # ranges of 4 lanes per expert column
     MoEConfig("bf16_select_n6_t700_warp_finish", 700, 128, 6, 2, 128, 1.1, "bf16", seed=21),
+    # the one-warp finish above 32 experts: 7 blocks, 8 expert columns per lane, drops
+    MoEConfig("bf16_select_n256_t200_warp_finish", 200, 128, 256, 4, 64, 1.0, "bf16", seed=22),
 ]
 
 
