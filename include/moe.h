@@ -297,6 +297,9 @@ typedef struct {
   int32_t launches;        /* kernel launches of one forward with T > 0 (T = 0: none) */
   int64_t capacity;        /* C without a valid-token mask; -1 for no limit */
   int64_t workspace_bytes; /* moe_workspace_size_ex(cfg, opts) */
+  int32_t routing_threads; /* threads per block of the routing-decision kernel */
+  int32_t routing_warp_finish; /* 1: the last routing block's per-expert scan, capacity,
+                              loss and expert layout run in one warp, 0: in the block */
 } moe_plan;
 
 /* Fill *plan for cfg and opts (NULL opts: the base layer). Returns MOE_OK,

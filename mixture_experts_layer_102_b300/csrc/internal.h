@@ -77,6 +77,25 @@ cudaError_t launch_route_select(const SelectArgs& a, int nblk, cudaStream_t stre
 // launch_route_select writes with blocks of ROUTE_FUSED_TOKENS tokens (a.part, a.ksplit
 // and a.tpw unused). `logits` [T][N] receives the logits with bias, or is null.
 constexpr int ROUTE_FUSED_TOKENS = 128;
+
+// The routing kernels' finish (the last block's per-expert scan, capacity, losses and
+// expert layout) runs in one warp when the layer has no mask and neither optional loss
+// and every lane holds its share of the per-block counts in registers: up to 32
+// experts, L = 32/np2(N) lanes share an expert column and each takes at most max_rows
+// block rows; above 32 experts a lane takes every block row of its columns, at most
+// max_rows. The fused kernel's lanes take up to 16 rows, the routing-decision kernel's
+// up to 8 (its 1024-thread blocks leave 64 registers).
+constexpr int FUSED_WARP_FINISH_ROWS = 16;
+constexpr int SELECT_WARP_FINISH_ROWS = 8;
+inline bool warp_finish_fits(int N, int nblk, bool plain, int max_rows) {
+  if (!plain) return false;
+  int np2 = 1;
+  while (np2 < N) np2 <<= 1;
+  return np2 <= 32 ? nblk <= max_rows * (32 / np2) : nblk <= max_rows;
+}
+// Threads per CTA of the fused routing kernel: four threads per token in the decisions
+// above 32 experts, two otherwise.
+inline int route_fused_threads(int N) { return N > 32 ? 512 : 256; }
 cudaError_t launch_route_fused(const SelectArgs& a, const void* x, const void* w_router, int H,
                                float* logits, uint32_t* status, cudaStream_t stream, bool pdl);
 

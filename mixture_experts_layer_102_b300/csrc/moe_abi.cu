@@ -567,6 +567,16 @@ int moe_describe(const moe_cfg* cfg, const moe_options* opts, int has_bias, moe_
   plan->launches = (p.fused ? 1 : 2) + (p.reroute ? 1 : 0) + 1 + 2 + 1;
   plan->capacity = p.C;
   plan->workspace_bytes = (int64_t)p.total;
+  // the routing kernel the forward launches: its finish and its threads per block
+  const bool plain = op.valid == nullptr && op.aux_kl == nullptr && op.aux_std2 == nullptr;
+  const int nblk = p.fused ? (p.T + ROUTE_FUSED_TOKENS - 1) / ROUTE_FUSED_TOKENS : p.n_sel_blocks;
+  plan->routing_threads = p.fused ? route_fused_threads(p.N) : SELECT_WARPS * 32;
+  plan->routing_warp_finish =
+      warp_finish_fits(p.N, nblk, plain,
+                       p.fused ? FUSED_WARP_FINISH_ROWS : SELECT_WARP_FINISH_ROWS) &&
+              !(p.fused && plan->routing_threads != 256)
+          ? 1
+          : 0;
   return MOE_OK;
 }
 

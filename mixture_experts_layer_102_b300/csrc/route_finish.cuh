@@ -255,25 +255,16 @@ __device__ inline void finish_routing(const SelectArgs& a, int nblk) {
   layout_experts(s_kept, Ntot, lay);
 }
 
-// The same finish for small layers in one warp, with no block barrier: no mask and
-// neither optional loss, and few enough blocks that every lane holds its rows of
-// counts and sums of P in registers (at most MAXR). Up to 32 experts, L = 32 / np2(N)
-// lanes share an expert column, each taking a contiguous range of block rows, and a
-// prefix over those ranges (shuffles) gives every block its base. Above 32 experts a
-// lane takes all rows of experts lane, lane + 32, ... one after another. Lane e then
-// holds expert e's totals (e, e + 32, ... above 32 experts), so the aux sum reduces
-// the same per-expert products in the same order as the block finish.
-// The kernels take the finish as a template argument chosen on the host, so each
-// carries the code of one finish only.
-template <int MAXR>
-inline bool warp_finish_fits(const SelectArgs& a, int nblk) {
-  if (a.valid != nullptr || a.aux_kl != nullptr || a.aux_std2 != nullptr) return false;
-  int np2 = 1;
-  while (np2 < a.N) np2 <<= 1;
-  return np2 <= 32 ? nblk <= MAXR * (32 / np2) : nblk <= MAXR;
-}
-
-// Called by warp 0 only, where warp_finish_fits<MAXR>() holds.
+// The same finish for small layers in one warp, with no block barrier, where
+// warp_finish_fits() holds (internal.h). Up to 32 experts, L = 32 / np2(N) lanes share
+// an expert column, each taking a contiguous range of block rows, and a prefix over
+// those ranges (shuffles) gives every block its base. Above 32 experts a lane takes
+// all rows of experts lane, lane + 32, ... one after another. Lane e then holds expert
+// e's totals (e, e + 32, ... above 32 experts), so the aux sum reduces the same
+// per-expert products in the same order as the block finish. The kernels take the
+// finish as a template argument chosen on the host, so each carries the code of one
+// finish only.
+// Called by warp 0 only; MAXR is the max_rows that warp_finish_fits() was given.
 template <int MAXR>
 __device__ inline void finish_routing_warp(const SelectArgs& a, int nblk) {
   __shared__ int32_t s_rows[MAX_EXPERTS];

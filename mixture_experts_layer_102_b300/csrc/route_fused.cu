@@ -45,7 +45,6 @@ constexpr int BK = 64;                          // 64 bf16 = one 128-byte swizzl
 constexpr int TOK = 128;                        // tokens per CTA (TMEM lanes)
 constexpr uint32_t A_BYTES = TOK * BK * 2;      // 16 KB
 constexpr int MAX_STAGES = 16;
-constexpr int WARP_FINISH_ROWS = 16;            // block rows per lane in the one-warp finish
 
 // Row stride (floats) of the tile's logits in shared memory: at least N + 1 and an odd
 // multiple of tpt (the threads per token), so the tpt threads of each of a warp's
@@ -385,7 +384,7 @@ route_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
   if (!is_last) return;
   __threadfence();
   if constexpr (WF) {
-    if (threadIdx.x < 32) finish_routing_warp<WARP_FINISH_ROWS>(a, gridDim.x);
+    if (threadIdx.x < 32) finish_routing_warp<FUSED_WARP_FINISH_ROWS>(a, gridDim.x);
   } else {
     finish_routing(a, gridDim.x);
   }
@@ -416,9 +415,10 @@ cudaError_t launch_route_fused(const SelectArgs& s, const void* x, const void* w
   // (same-call A/B on the fine-grained layer: route stage 48.5 -> 45.1 us); the
   // smaller layers were no faster with them. With 32 or more blocks the one-warp
   // finish fits up to 16 experts.
-  const bool wf = route::warp_finish_fits<WARP_FINISH_ROWS>(s, nblk);
-  const int variant = wf ? 0 : s.N > 32 ? 2 : 1;
-  const int nthreads = variant == 2 ? 512 : 256;
+  const bool plain = s.valid == nullptr && s.aux_kl == nullptr && s.aux_std2 == nullptr;
+  const bool wf = warp_finish_fits(s.N, nblk, plain, FUSED_WARP_FINISH_ROWS);
+  const int nthreads = route_fused_threads(s.N);
+  const int variant = wf && nthreads == 256 ? 0 : nthreads == 512 ? 2 : 1;
   auto kernel = variant == 0 ? route_fused_kernel<true, 256>
               : variant == 1 ? route_fused_kernel<false, 256>
                              : route_fused_kernel<false, 512>;

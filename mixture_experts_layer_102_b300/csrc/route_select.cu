@@ -52,7 +52,6 @@ using namespace route;
 
 constexpr int WARPS = SELECT_WARPS;  // 32
 constexpr int MAX_TPW = 4;           // tokens per warp whose ranks stay in registers
-constexpr int WARP_FINISH_ROWS = 8;  // block rows per lane in the one-warp finish
 
 // OPT: the valid-token mask or the variance loss may be in use (read at run time);
 // without it those branches are compiled out of the base layer's kernel.
@@ -267,7 +266,7 @@ __global__ void __launch_bounds__(1024) route_select_kernel(SelectArgs a) {
   if (!is_last) return;
   __threadfence();
   if constexpr (WF) {
-    if (threadIdx.x < 32) finish_routing_warp<WARP_FINISH_ROWS>(a, gridDim.x);
+    if (threadIdx.x < 32) finish_routing_warp<SELECT_WARP_FINISH_ROWS>(a, gridDim.x);
   } else {
     finish_routing(a, gridDim.x);
   }
@@ -280,9 +279,9 @@ cudaError_t launch_route_select(const SelectArgs& a, int nblk, cudaStream_t stre
   if (a.T == 0) return cudaSuccess;
   const size_t smem = (size_t)WARPS * a.N * 8;  // counters and P sums of every warp
   const bool opt = a.valid != nullptr || a.aux_std2 != nullptr;
-  // options that need the block finish (a mask, the variance loss) exclude the warp one
+  const bool plain = !opt && a.aux_kl == nullptr;  // the one-warp finish computes no KL
   auto kernel = opt ? route_select_kernel<true, false>
-                : route::warp_finish_fits<WARP_FINISH_ROWS>(a, nblk)
+                : warp_finish_fits(a.N, nblk, plain, SELECT_WARP_FINISH_ROWS)
                     ? route_select_kernel<false, true>
                     : route_select_kernel<false, false>;
   const cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(kernel), smem);

@@ -95,7 +95,8 @@ class MoEPlan(ctypes.Structure):
     _fields_ = [("fused_routing", ctypes.c_int32), ("routing_block", ctypes.c_int32),
                 ("router_ksplit", ctypes.c_int32), ("gemm1_tile_rows", ctypes.c_int32),
                 ("gemm2_tile_rows", ctypes.c_int32), ("launches", ctypes.c_int32),
-                ("capacity", ctypes.c_int64), ("workspace_bytes", ctypes.c_int64)]
+                ("capacity", ctypes.c_int64), ("workspace_bytes", ctypes.c_int64),
+                ("routing_threads", ctypes.c_int32), ("routing_warp_finish", ctypes.c_int32)]
 
 
 class MoEError(RuntimeError):

@@ -239,6 +239,33 @@ def test_describe_fused_threshold_and_options():
     assert _plan(configs.BF16_T4096, sh)["workspace_bytes"] == moe.workspace_size(c, sh)
 
 
+def test_describe_routing_finish_and_threads():
+    import torch
+    fin = lambda p: (p["routing_threads"], p["routing_warp_finish"])
+    # fused kernel: one-warp finish while 32/np2(N) lanes x 16 rows cover the blocks
+    assert fin(_plan(configs.BF16_T4096)) == (256, 1)            # N 16: 2 lanes, 32 blocks
+    assert fin(_plan(configs.BF16_T4096, T=4097)) == (256, 0)    # 33 blocks
+    assert fin(_plan(configs.MIXTRAL_T8192)) == (256, 1)         # N 8: 4 lanes, 64 blocks
+    assert fin(_plan(configs.MIXTRAL_T8192, T=8193)) == (256, 0)
+    assert fin(_plan(configs.BF16_T4096, N=17)) == (256, 0)      # np2 32: one lane, 16 rows
+    # above 32 experts the fused kernel runs four threads per token and the block finish
+    assert fin(_plan(configs.FINEGRAINED_T16384)) == (512, 0)
+    assert fin(_plan(configs.BF16_T4096, N=33)) == (512, 0)
+    # the routing-decision kernel (1024 threads): 8 rows per lane, any N
+    assert fin(_plan(configs.DECODE_T64)) == (1024, 1)           # N 100: 2 blocks
+    assert fin(_plan(configs.BF16_T4096, T=200, N=256, k=4)) == (1024, 1)   # 7 blocks
+    assert fin(_plan(configs.BF16_T4096, T=257, N=256, k=4)) == (1024, 0)   # 9 blocks
+    assert fin(_plan(configs.TINY_F32)) == (1024, 1)
+    # a mask or an optional loss keeps the block finish
+    one = torch.zeros(1, dtype=torch.float32)
+    mask = torch.ones(configs.BF16_T4096.T, dtype=torch.uint8)
+    for o in (moe.Options(aux_kl=one), moe.Options(aux_std2=one), moe.Options(valid_mask=mask)):
+        assert fin(_plan(configs.BF16_T4096, o)) == (256, 0)
+        assert fin(_plan(configs.DECODE_T64, o))[1] == 0
+    # shared experts and rerouting do not change the choice
+    assert fin(_plan(configs.BF16_T4096, moe.Options(n_shared=2, reroute=True))) == (256, 1)
+
+
 def test_describe_rejects_bad_arguments():
     lib = moe.library()
     plan = moe.MoEPlan()
