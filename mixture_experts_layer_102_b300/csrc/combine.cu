@@ -16,8 +16,11 @@
 namespace moe {
 namespace {
 
-template <typename TIo>
-__global__ void __launch_bounds__(256)
+// MINB: blocks per SM the registers are capped for. 3 (at most 85 registers) keeps 24
+// warps' loads in flight per SM on the large layers; a small batch of a few blocks runs
+// faster uncapped.
+template <typename TIo, int MINB>
+__global__ void __launch_bounds__(256, MINB)
 combine_kernel(const TIo* __restrict__ ye, const int32_t* __restrict__ slot_row,
                const float* __restrict__ w, int T, int k, int S, int H,
                TIo* __restrict__ out) {
@@ -102,6 +105,8 @@ combine_kernel(const TIo* __restrict__ ye, const int32_t* __restrict__ slot_row,
   }
 }
 
+constexpr int COMBINE_CAPPED_MIN_TOKENS = 4096;
+
 }  // namespace
 
 cudaError_t launch_combine(int dtype, const void* ye, const int32_t* slot_row, const float* w,
@@ -109,11 +114,18 @@ cudaError_t launch_combine(int dtype, const void* ye, const int32_t* slot_row, c
                            bool pdl) {
   if (T == 0) return cudaSuccess;
   const dim3 grid((T + 7) / 8), block(256);
+  // Same-call A/B: capped registers took the Mixtral-shaped combine 48.4 -> 44.5 us and
+  // the fine-grained one 36.3 -> 31.5 us, left T = 4096 unchanged and slowed the
+  // 64-token decode batch 10.8 -> 12.2 us (its 8 blocks gain nothing from occupancy).
   if (dtype == 1)
-    return launch_kernel(combine_kernel<__nv_bfloat16>, grid, block, 0, stream, pdl,
-                         static_cast<const __nv_bfloat16*>(ye), slot_row, w, T, k, S, H,
-                         static_cast<__nv_bfloat16*>(out));
-  return launch_kernel(combine_kernel<float>, grid, block, 0, stream, pdl,
+    return T >= COMBINE_CAPPED_MIN_TOKENS
+               ? launch_kernel(combine_kernel<__nv_bfloat16, 3>, grid, block, 0, stream, pdl,
+                               static_cast<const __nv_bfloat16*>(ye), slot_row, w, T, k, S, H,
+                               static_cast<__nv_bfloat16*>(out))
+               : launch_kernel(combine_kernel<__nv_bfloat16, 1>, grid, block, 0, stream, pdl,
+                               static_cast<const __nv_bfloat16*>(ye), slot_row, w, T, k, S, H,
+                               static_cast<__nv_bfloat16*>(out));
+  return launch_kernel(combine_kernel<float, 1>, grid, block, 0, stream, pdl,
                        static_cast<const float*>(ye), slot_row, w, T, k, S, H,
                        static_cast<float*>(out));
 }
