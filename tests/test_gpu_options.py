@@ -57,12 +57,13 @@ def _max_ratio(y, r):
     return float(np.abs(y - r).max() / np.abs(r).max())
 
 
-def run_opts(cfg, inp, n_shared=0, activation="swiglu", mask=None, reroute=False):
+def run_opts(cfg, inp, n_shared=0, activation="swiglu", mask=None, reroute=False,
+             losses=True):
     c = moe.cfg_from(cfg)
     dev = moe.to_device(inp)
     vm = None if mask is None else torch.from_numpy(mask).cuda()
-    kl = torch.full((1,), -7.0, device="cuda")
-    s2 = torch.full((1,), -7.0, device="cuda")
+    kl = torch.full((1,), -7.0, device="cuda") if losses else None
+    s2 = torch.full((1,), -7.0, device="cuda") if losses else None
     opts = moe.Options(n_shared, activation, vm, kl, s2, reroute)
     ws = moe.make_workspace(c, options=opts)
     routing = moe.new_routing(c)
@@ -73,8 +74,8 @@ def run_opts(cfg, inp, n_shared=0, activation="swiglu", mask=None, reroute=False
     g = {k: getattr(routing, k).cpu().numpy() for k in
          ("topk_idx", "topk_w", "aux_loss", "drop_mask", "expert_counts", "kept_counts")}
     g["out"] = out.float().cpu().numpy()
-    g["aux_kl"] = float(kl.item())
-    g["aux_std2"] = float(s2.item())
+    g["aux_kl"] = float(kl.item()) if losses else None
+    g["aux_std2"] = float(s2.item()) if losses else None
     return g, (c, dev, ws, opts)
 
 
@@ -134,11 +135,15 @@ def compare_opts(cfg, g, ref, mask, n_shared):
     else:
         assert g["drop_mask"][v].sum() == 0
 
-    if math.isinf(kl_ref):
+    if g["aux_kl"] is None:  # the optional losses were not asked for
+        pass
+    elif math.isinf(kl_ref):
         assert g["aux_kl"] == math.inf
     else:
         assert abs(g["aux_kl"] - kl_ref) <= TOL_KL * max(1.0, abs(kl_ref)), (g["aux_kl"], kl_ref)
-    if math.isnan(ref.aux_std2):
+    if g["aux_std2"] is None:
+        pass
+    elif math.isnan(ref.aux_std2):
         assert math.isnan(g["aux_std2"])
     else:
         assert abs(g["aux_std2"] - ref.aux_std2) <= TOL_STD2 * abs(ref.aux_std2) + 1e-12, \
@@ -165,10 +170,11 @@ def compare_opts(cfg, g, ref, mask, n_shared):
     return info
 
 
-def check_opts(cfg, n_shared=0, activation="swiglu", seq_len=None, token_sample=None):
+def check_opts(cfg, n_shared=0, activation="swiglu", seq_len=None, token_sample=None,
+               losses=True):
     inp = inputs.make_inputs(cfg, n_shared=n_shared)
     mask = None if seq_len is None else inputs.make_valid_mask(cfg.T, seq_len, cfg.seed)
-    g, _ = run_opts(cfg, inp, n_shared, activation, mask)
+    g, _ = run_opts(cfg, inp, n_shared, activation, mask, losses=losses)
     ref = oracle_opts(cfg, inp, n_shared, activation, mask, token_sample)
     return compare_opts(cfg, g, ref, mask, n_shared)
 
@@ -184,9 +190,9 @@ CASES = [
                seed=50, zipf_bias=True), 1, "swiglu", 500),
     (MoEConfig("bf16_fused_n1_k1_t4096", 4096, 128, 1, 1, 64, None, "bf16", seed=39), 0,
      "swiglu", None),
-    # one-warp routing finish: 4 lanes per expert column over ragged ranges of the 40
-    # blocks, with shared experts and capacity drops
-    (MoEConfig("bf16_fused_n5_t5000_warp_finish", 5000, 128, 5, 2, 64, 1.1, "bf16", seed=52,
+    # few experts over 40 blocks with shared experts and capacity drops (the optional
+    # losses asked for here keep the block finish; see the one-warp test below)
+    (MoEConfig("bf16_fused_n5_t5000", 5000, 128, 5, 2, 64, 1.1, "bf16", seed=52,
                zipf_bias=True), 2, "swiglu", None),
     (MoEConfig("bf16_fused_k32_n64_masked_shared", 4100, 64, 64, 32, 64, 0.9, "bf16", seed=40,
                zipf_bias=True), 2, "gelu", 300),
@@ -225,6 +231,26 @@ CASES = [
 def test_options_elementwise(case):
     cfg, n_shared, act, seq_len = case
     check_opts(cfg, n_shared, act, seq_len)
+
+
+# Shared experts without a mask or the optional losses: the routing kernel finishes in
+# one warp, on the fused path (4 lanes per expert over ragged ranges of 40 blocks) and
+# on the two-launch path (22 blocks of 32 tokens).
+WARP_FINISH_SHARED = [
+    (MoEConfig("bf16_fused_n5_t5000_s2_warp_finish", 5000, 128, 5, 2, 64, 1.1, "bf16",
+               seed=53, zipf_bias=True), 2),
+    (MoEConfig("bf16_select_n6_t700_s1_warp_finish", 700, 128, 6, 2, 128, 1.1, "bf16",
+               seed=54), 1),
+]
+
+
+@pytest.mark.parametrize("case", WARP_FINISH_SHARED, ids=lambda c: c[0].name)
+def test_shared_experts_with_the_one_warp_finish(case):
+    cfg, n_shared = case
+    plan = moe.describe(moe.cfg_from(cfg), moe.Options(n_shared=n_shared),
+                        has_bias=cfg.zipf_bias)
+    assert plan["routing_warp_finish"] == 1
+    check_opts(cfg, n_shared, "swiglu", None, losses=False)
 
 
 def test_bench_shape_with_every_option_sampled():
