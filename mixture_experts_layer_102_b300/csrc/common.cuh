@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
 #include <mutex>
 
 namespace moe {
@@ -86,18 +87,19 @@ inline cudaError_t ensure_dynamic_smem(const void* kernel, size_t bytes) {
 
 // Opt-in shared memory per block of the current device (cached per device).
 inline cudaError_t smem_optin_bytes(size_t* out) {
-  static int cached[64] = {0};
+  static std::atomic<int> cached[64];  // 0 until the first query on that device
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev >= 0 && dev < 64 && cached[dev] > 0) {
-    *out = (size_t)cached[dev];
+  const int c = dev >= 0 && dev < 64 ? cached[dev].load(std::memory_order_relaxed) : 0;
+  if (c > 0) {
+    *out = (size_t)c;
     return cudaSuccess;
   }
   int v = 0;
   e = cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
   if (e != cudaSuccess) return e;
-  if (dev >= 0 && dev < 64) cached[dev] = v;
+  if (dev >= 0 && dev < 64) cached[dev].store(v, std::memory_order_relaxed);
   *out = (size_t)v;
   return cudaSuccess;
 }

@@ -465,10 +465,11 @@ int g_test_skip_kchunk = -1;  // see moe_test_withhold_gemm_load
 // Work units (CTAs, or CTA pairs) that can be resident at once: the grid size.
 template <int EPI, int CG>
 int grid_units() {
-  static int cached[64] = {0};
+  static std::atomic<int> cached[64];  // 0 until the first launch on that device
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && cached[dev] > 0) return cached[dev];
+  const int c = dev >= 0 && dev < 64 ? cached[dev].load(std::memory_order_relaxed) : 0;
+  if (c > 0) return c;
   int sms = 0;
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   int n = sms > 0 ? sms / CG : 1;
@@ -492,7 +493,7 @@ int grid_units() {
     cudaGetLastError();
   }
   if (n < 1) n = 1;
-  if (dev >= 0 && dev < 64) cached[dev] = n;
+  if (dev >= 0 && dev < 64) cached[dev].store(n, std::memory_order_relaxed);
   return n;
 }
 
